@@ -1,0 +1,173 @@
+"""Plain float64 CPU oracle for speculative-decoding verify-and-commit and the
+n-gram proposer -- TEST INFRASTRUCTURE.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's
+CPU-baseline leg import this package. The CUDA library never uses it and the
+two share no code: the oracle is ``oracle.c`` (float64, one row at a time,
+written from the pages' algorithm), compiled with gcc into ``liboracle.so``
+beside it and called through ctypes with numpy arrays.
+
+What each function follows is cited in ``oracle.c``. Every function here is
+pinned by ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+FP32, BF16 = 0, 1
+MODE_SAMPLE, MODE_GREEDY = 0, 1
+MARGIN_EPS = 1e-6
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (plain gcc, IEEE float64: no fast-math,
+    no FMA contraction, so x86 and Arm give the same results)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call([
+            "gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+            "-shared", "-o", tmp, _SRC, "-lm", "-lpthread",
+        ])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.oracle_softmax.argtypes = [P, i32, i32, f64, P]
+        lib.oracle_softmax.restype = f64
+        lib.oracle_argmax.argtypes = [P, i32, i32]
+        lib.oracle_argmax.restype = i32
+        lib.oracle_inverse_cdf.argtypes = [P, i32, f64, P]
+        lib.oracle_inverse_cdf.restype = i32
+        lib.oracle_spec_verify.argtypes = [P, P, i32, i32, i32, P, P, P, P, f64,
+                                           P, P, P, P, P, P, i32]
+        lib.oracle_spec_verify.restype = i32
+        lib.oracle_ngram_propose.argtypes = [P, i64, P, i32, i32, i32, i32, P, P, P]
+        lib.oracle_ngram_propose.restype = i32
+        lib.oracle_default_threads.argtypes = []
+        lib.oracle_default_threads.restype = i32
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _logits(z):
+    """float32 array -> (array, FP32); uint16 array of bf16 bit patterns -> (array, BF16)."""
+    z = np.ascontiguousarray(z)
+    if z.dtype == np.float32:
+        return z, FP32
+    if z.dtype == np.uint16:
+        return z, BF16
+    raise TypeError("logits must be float32 or uint16 (bf16 bit patterns)")
+
+
+def default_threads() -> int:
+    return int(_load().oracle_default_threads())
+
+
+def softmax(z, T: float = 1.0) -> np.ndarray:
+    """Temperature softmax of one logit row, float64."""
+    z, dt = _logits(z)
+    out = np.empty(z.shape[-1], np.float64)
+    _load().oracle_softmax(_ptr(z), dt, z.shape[-1], float(T), _ptr(out))
+    return out
+
+
+def argmax(z) -> int:
+    """First index of the maximal logit."""
+    z, dt = _logits(z)
+    return int(_load().oracle_argmax(_ptr(z), dt, z.shape[-1]))
+
+
+def inverse_cdf(r, u: float):
+    """(index, margin) of the inverse-CDF draw from unnormalised weights r."""
+    r = np.ascontiguousarray(r, np.float64)
+    m = np.zeros(1, np.float64)
+    k = _load().oracle_inverse_cdf(_ptr(r), r.shape[0], float(u), _ptr(m))
+    return int(k), float(m[0])
+
+
+@dataclass
+class VerifyResult:
+    out_tokens: np.ndarray  # [R_t] int32; request b's tokens at cu_draft[b]+b
+    out_len: np.ndarray     # [B] int32
+    out_probs: np.ndarray   # [R_t, 2] float64
+    margin: np.ndarray      # [R_t] float64, smallest decision margin of the row (inf if none)
+    rho: np.ndarray         # [R_t] float64, min(1, p/q) of tested sampling rows (nan otherwise)
+    stop: np.ndarray        # [B] int32
+
+    def flagged_rows(self) -> np.ndarray:
+        return self.margin < MARGIN_EPS
+
+
+def spec_verify(target, draft, draft_tokens, cu_draft, uniforms, temperature: float,
+                mode=None, nthreads: int = 0) -> VerifyResult:
+    """Verify-and-commit for a packed batch (layout as the CUDA library's).
+
+    target: [R_t, V] float32 or uint16(bf16); draft: [R_d, V] same dtype or None
+    (one-hot q); draft_tokens: [R_d] int32; cu_draft: [B+1] int32; uniforms:
+    [R_t, 2] float32; mode: [B] uint8 (0 sample, 1 greedy) or None.
+    """
+    target, dt = _logits(target)
+    V = target.shape[-1]
+    if draft is not None:
+        draft, dt2 = _logits(draft)
+        assert dt2 == dt and draft.shape[-1] == V
+    draft_tokens = np.ascontiguousarray(draft_tokens, np.int32)
+    cu_draft = np.ascontiguousarray(cu_draft, np.int32)
+    uniforms = np.ascontiguousarray(uniforms, np.float32)
+    B = cu_draft.shape[0] - 1
+    R_t = int(cu_draft[-1]) + B
+    assert target.shape[0] >= R_t and uniforms.shape[0] >= R_t
+    if mode is not None:
+        mode = np.ascontiguousarray(mode, np.uint8)
+    out_tokens = np.full(R_t, -1, np.int32)
+    out_len = np.zeros(B, np.int32)
+    out_probs = np.full((R_t, 2), np.nan, np.float64)
+    margin = np.full(R_t, np.inf, np.float64)
+    rho = np.full(R_t, np.nan, np.float64)
+    stop = np.zeros(B, np.int32)
+    st = _load().oracle_spec_verify(
+        _ptr(target), _ptr(draft), dt, V, B, _ptr(draft_tokens), _ptr(cu_draft), _ptr(mode),
+        _ptr(uniforms), float(temperature), _ptr(out_tokens), _ptr(out_len), _ptr(out_probs),
+        _ptr(margin), _ptr(rho), _ptr(stop), int(nthreads))
+    if st != 0:
+        raise ValueError(f"oracle_spec_verify: invalid request data (code {st})")
+    return VerifyResult(out_tokens, out_len, out_probs, margin, rho, stop)
+
+
+def ngram_propose(histories, hist_len, min_n: int, max_n: int, max_tokens: int):
+    """(out_tokens [B, max_tokens], out_count [B], out_n [B]) for int32 histories [B, stride]."""
+    histories = np.ascontiguousarray(histories, np.int32)
+    if histories.ndim == 1:
+        histories = histories[None, :]
+    hist_len = np.ascontiguousarray(hist_len, np.int32)
+    B, stride = histories.shape
+    out = np.full((B, max(max_tokens, 0)), -1, np.int32)
+    cnt = np.zeros(B, np.int32)
+    nn = np.zeros(B, np.int32)
+    st = _load().oracle_ngram_propose(_ptr(histories), stride, _ptr(hist_len), B, int(min_n),
+                                      int(max_n), int(max_tokens), _ptr(out), _ptr(cnt), _ptr(nn))
+    if st != 0:
+        raise ValueError("oracle_ngram_propose: history length out of range")
+    return out, cnt, nn
