@@ -1,0 +1,195 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-decoding
+ * verify-and-commit library (libspecverify.so).
+ *
+ * What the library computes is the verify-and-commit step of speculative
+ * decoding and the model-free n-gram proposer, as these pages define them:
+ *
+ *   "Draft Model（草稿模型）" (compassingai.com), §2 "接受-拒绝准则" and the
+ *   box "算法：Speculative Decoding (一步)": for draft slots i = 1..K in
+ *   order, accept the draft token x̂_i with probability min(1, p(x̂_i)/q(x̂_i));
+ *   at the first rejection emit a token drawn from norm(max(0, p - q)) and
+ *   stop; if all K are accepted emit one more token drawn from p_{K+1}.
+ *   Each round emits 1..K+1 tokens.
+ *
+ *   "投机解码从零实现" (CSDN), §3.2 "算法的数学推导" and §4.3 "验证器实现":
+ *   both logit rows are divided by the temperature before the softmax;
+ *   p'(x) = max(0, p(x) - q(x)) / Z with Z = sum_x max(0, p(x) - q(x));
+ *   a draft probability q(x̂) <= 0 rejects.
+ *
+ *   "Speculative Decoding在分布式推理中的应用", §二 "推测解码的工作流程":
+ *   strict verification accepts iff the draft token equals the target's own
+ *   choice (with greedy decoding: the argmax).
+ *
+ *   "5.2 Draft 模型与无模型方案：怎样便宜地猜得更准", §4 "N-gram" and §6
+ *   "动手实验": the prompt-lookup proposer; §4.3: a copied proposal is the
+ *   one-hot distribution q(y) = 1 on the proposed token.
+ *
+ * Conventions for every entry point:
+ *   - Array arguments are DEVICE pointers owned by the caller. The library
+ *     allocates no device memory; scratch space is the caller's workspace.
+ *   - Work is enqueued asynchronously on `cuda_stream` (a cudaStream_t; NULL
+ *     is the legacy default stream). Results are valid once the stream has
+ *     reached that point.
+ *   - Errors visible on the host (NULL where a pointer is required, bad sizes,
+ *     misaligned pointers, temperature <= 0) return SV_ERR_INVALID_ARG
+ *     before anything is launched. A failed launch returns SV_ERR_CUDA.
+ *   - Errors that depend on device data (offsets, token ids, rows without a
+ *     finite logit) are found by the kernels, which never trap: they set bits
+ *     in a status word inside the workspace (SV_DATA_* below), keep every
+ *     memory access in bounds, and finish. sv_check_status() reads and clears
+ *     that word. Outputs of a call whose status word is non-zero (other than
+ *     the informational SV_DATA_DEGENERATE_RESIDUAL bit) are unspecified.
+ *   - Logits must be finite or -inf (a masked token); NaN and +inf are not
+ *     supported. Each row needs at least one finite logit.
+ *
+ * Packed ragged layout (B requests, request b has K_b >= 0 draft tokens):
+ *   cu_draft[B+1]        exclusive prefix sums of K_b; cu_draft[0] = 0.
+ *   R_d = cu_draft[B]    draft rows;  R_t = R_d + B  target rows.
+ *   draft slot (b, i), i < K_b:   draft row / draft token at cu_draft[b] + i.
+ *   target row (b, i), i <= K_b:  at cu_draft[b] + b + i. Row i is the
+ *       target's distribution for draft slot i; row K_b is the bonus slot.
+ *   Logit matrices are row-major [rows, V] with row stride V elements.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1,   /* rejected on the host before any launch */
+  SV_ERR_CUDA = 2,          /* a CUDA runtime call or launch failed */
+  SV_ERR_TIMEOUT = 3,       /* reserved: a bounded device-side wait gave up */
+  SV_ERR_UNIMPLEMENTED = 4, /* reserved */
+  SV_ERR_DATA = 5           /* sv_check_status found device-side data errors */
+} sv_status;
+
+typedef enum { SV_FP32 = 0, SV_BF16 = 1 } sv_dtype;
+
+enum { SV_MODE_SAMPLE = 0, SV_MODE_GREEDY = 1 };
+
+/* Bits of the device status word (sv_check_status). */
+#define SV_DATA_BAD_OFFSETS 0x1u   /* cu_draft[0] != 0, decreasing, or R_t beyond the workspace */
+#define SV_DATA_BAD_TOKEN 0x2u     /* a draft token outside [0, V) (the slot is rejected) */
+#define SV_DATA_EMPTY_ROW 0x4u     /* a sampled row without any finite logit */
+#define SV_DATA_BAD_MODE 0x8u      /* mode[b] not SAMPLE or GREEDY (treated as SAMPLE) */
+#define SV_DATA_DEGENERATE_RESIDUAL 0x10u /* informational: residual mass 0 after a reject; drew from p */
+
+/*
+ * Bytes of workspace spec_verify / spec_verify_greedy need for B requests
+ * and R_t target rows. The workspace must be 16-byte aligned and zero-filled
+ * before its first use; every call leaves its counters at zero again, so
+ * calls in stream order may reuse it without clearing. Calls that may run
+ * concurrently (other streams) need distinct workspaces.
+ */
+size_t spec_verify_workspace_size(int32_t B, int32_t R_t);
+
+/*
+ * Lossless verify-and-commit ("Draft Model（草稿模型）", §2 and the algorithm
+ * box; "投机解码从零实现" §3.2/§4.3).
+ *
+ *   target_logits  [R_t, V] dtype.
+ *   draft_logits   [R_d, V] dtype, or NULL: every proposal is one-hot
+ *                  (q = e_x̂, "5.2 Draft 模型与无模型方案" §4.3); then
+ *                  min(1, p/q) = p(x̂) and the residual is p without x̂.
+ *   dtype          SV_FP32 or SV_BF16 for both logit matrices.
+ *   V >= 1, B >= 0 (B == 0 is a no-op).
+ *   draft_tokens   [R_d] int32 proposed tokens (may be NULL when R_d == 0).
+ *   cu_draft       [B+1] int32 offsets (see the layout above).
+ *   mode           [B] uint8 SV_MODE_* per request, or NULL (all SAMPLE).
+ *                  GREEDY requests use strict verification (as
+ *                  spec_verify_greedy) and ignore draft rows and uniforms.
+ *   uniforms       [R_t, 2] float32 in [0, 1): per target row, u (accept
+ *                  test of that row's draft slot) and u' (the draw made at
+ *                  that row, if it is the request's stop row).
+ *   temperature    T > 0: p = softmax(z_target / T), q = softmax(z_draft / T).
+ *   out_tokens     [R_t] int32: request b's committed tokens at
+ *                  cu_draft[b] + b + j, j < out_len[b]; other entries are
+ *                  left untouched.
+ *   out_len        [B] int32 in [1, K_b + 1].
+ *   out_probs      [R_t, 2] float32 or NULL. Draft slot rows get
+ *                  (p(x̂_i), q(x̂_i)) for every i < K_b (also after the stop);
+ *                  the bonus-slot row K_b gets (p_s(y), q_s(y)) of the final
+ *                  token y drawn at the stop row s (q_s(y) = 0 for a bonus
+ *                  draw). GREEDY requests get (-1, -1).
+ *   workspace      device scratch, >= spec_verify_workspace_size(B, R_t)
+ *                  bytes, 16-byte aligned, zero-filled before first use.
+ *
+ * Decision rule: accept slot i iff u_i < min(1, p(x̂_i)/q(x̂_i)), with
+ * q(x̂_i) = 0 rejecting. The draw at stop row s takes the smallest k with
+ * sum_{x<=k} r_x > u'_s * sum_x r_x in vocabulary order, r = max(0, p - q)
+ * after a rejection and r = p for the bonus draw.
+ */
+sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                      int32_t V, int32_t B, const int32_t* draft_tokens,
+                      const int32_t* cu_draft, const uint8_t* mode, const float* uniforms,
+                      float temperature, int32_t* out_tokens, int32_t* out_len,
+                      float* out_probs, void* workspace, size_t workspace_bytes,
+                      void* cuda_stream);
+
+/*
+ * Strict (greedy) verify-and-commit ("Speculative Decoding在分布式推理中的应用",
+ * §二, strict verification): accept slot i iff x̂_i equals the argmax of
+ * target row i (lowest index among ties); at the first mismatch, or at the
+ * bonus row, emit that row's argmax. Bit-exact; no temperature, no
+ * uniforms. Arguments as for spec_verify.
+ */
+sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype, int32_t V, int32_t B,
+                             const int32_t* draft_tokens, const int32_t* cu_draft,
+                             int32_t* out_tokens, int32_t* out_len, void* workspace,
+                             size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * N-gram / prompt-lookup proposer ("5.2 Draft 模型与无模型方案", §4.1 and §6):
+ * for n = min(max_n, L) down to min_n, take the tail h[L-n, L) of the
+ * history and find the most recent earlier start s, 0 <= s <= L-2n-1, with
+ * h[s, s+n) equal to the tail (the match ends before the tail starts and
+ * leaves a non-empty continuation); propose h[s+n, min(s+n+max_tokens, L-n)).
+ * Without a match for any n: out_n = 0 and out_count = 0.
+ *
+ *   histories   [B, hist_stride] int32 token ids; history b holds hist_len[b]
+ *               tokens (clamped to [0, hist_stride]).
+ *   min_n >= 1, max_n >= min_n, max_tokens >= 0, B >= 0.
+ *   out_tokens  [B, max_tokens] int32: proposal b in row b; entries past
+ *               out_count[b] are set to -1.
+ *   out_count   [B] int32 proposal lengths.
+ *   out_n       [B] int32 matched window length (0 if none).
+ * Bit-exact. No workspace.
+ */
+sv_status ngram_propose(const int32_t* histories, int64_t hist_stride, const int32_t* hist_len,
+                        int32_t B, int32_t min_n, int32_t max_n, int32_t max_tokens,
+                        int32_t* out_tokens, int32_t* out_count, int32_t* out_n,
+                        void* cuda_stream);
+
+/*
+ * Glue from ngram_propose to spec_verify: cu_draft[B+1] = exclusive prefix
+ * sums of counts[B] (clamped to [0, max_tokens]), and the proposals of
+ * tokens[B, max_tokens] packed to packed[cu_draft[b] + i] (capacity
+ * B * max_tokens). One launch on the stream.
+ */
+sv_status sv_pack_drafts(const int32_t* tokens, const int32_t* counts, int32_t B,
+                         int32_t max_tokens, int32_t* cu_draft, int32_t* packed,
+                         void* cuda_stream);
+
+/*
+ * Synchronizes `cuda_stream`, reads the status word of `workspace` into
+ * *out_bits (SV_DATA_* bits) and clears it. Returns SV_OK when no error bit
+ * is set (SV_DATA_DEGENERATE_RESIDUAL alone is informational), SV_ERR_DATA
+ * otherwise, or SV_ERR_CUDA / SV_ERR_INVALID_ARG.
+ */
+sv_status sv_check_status(void* workspace, void* cuda_stream, uint32_t* out_bits);
+
+/* Static, human-readable name of a status code. */
+const char* sv_status_string(sv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,201 @@
+"""Python binding of libspecverify.so, with the C ABI's names.
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Tensors must be CUDA tensors; there is no CPU path, and a missing library is an
+error, not a fallback. PyTorch supplies device memory and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+import torch
+
+from .build import LIB_PATH, ROOT
+
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_CUDA, SV_ERR_TIMEOUT, SV_ERR_UNIMPLEMENTED, SV_ERR_DATA = range(6)
+SV_FP32, SV_BF16 = 0, 1
+SV_MODE_SAMPLE, SV_MODE_GREEDY = 0, 1
+SV_DATA_BAD_OFFSETS = 0x1
+SV_DATA_BAD_TOKEN = 0x2
+SV_DATA_EMPTY_ROW = 0x4
+SV_DATA_BAD_MODE = 0x8
+SV_DATA_DEGENERATE_RESIDUAL = 0x10
+
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+        self.status = status
+
+
+def load() -> ctypes.CDLL:
+    """Load the CUDA library (built in-tree by build.build_library())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it first "
+            "(speculative_decoding_verification_27_gb300.build.build_library())")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.spec_verify_workspace_size.argtypes = [i32, i32]
+    lib.spec_verify_workspace_size.restype = sz
+    lib.spec_verify.argtypes = [P, P, ctypes.c_int, i32, i32, P, P, P, P, f32, P, P, P, P, sz, P]
+    lib.spec_verify.restype = ctypes.c_int
+    lib.spec_verify_greedy.argtypes = [P, ctypes.c_int, i32, i32, P, P, P, P, P, sz, P]
+    lib.spec_verify_greedy.restype = ctypes.c_int
+    lib.ngram_propose.argtypes = [P, i64, P, i32, i32, i32, i32, P, P, P, P]
+    lib.ngram_propose.restype = ctypes.c_int
+    lib.sv_pack_drafts.argtypes = [P, P, i32, i32, P, P, P]
+    lib.sv_pack_drafts.restype = ctypes.c_int
+    lib.sv_check_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.sv_check_status.restype = ctypes.c_int
+    lib.sv_status_string.argtypes = [ctypes.c_int]
+    lib.sv_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def header_functions() -> list:
+    """Names of the functions declared in include/spec_verify.h."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(\w+)\s*\(", text)) - {"defined", "if"})
+
+
+def status_string(status: int) -> str:
+    return load().sv_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != SV_OK:
+        raise SpecVerifyError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("spec_verify tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("spec_verify tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SV_FP32
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    raise ValueError("logits must be float32 or bfloat16")
+
+
+def spec_verify_workspace_size(B: int, R_t: int) -> int:
+    return int(load().spec_verify_workspace_size(int(B), int(R_t)))
+
+
+def new_workspace(B: int, R_t: int, device="cuda") -> torch.Tensor:
+    """Zero-filled workspace (the library leaves it zeroed after each call)."""
+    return torch.zeros(spec_verify_workspace_size(B, R_t), dtype=torch.uint8, device=device)
+
+
+def spec_verify(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor,
+                cu_draft: torch.Tensor, uniforms: torch.Tensor, temperature: float,
+                mode: Optional[torch.Tensor] = None, *, out_tokens=None, out_len=None,
+                out_probs=None, want_probs: bool = True, workspace=None, stream=None):
+    """Lossless verify-and-commit. Returns (out_tokens, out_len, out_probs)."""
+    lib = load()
+    B = cu_draft.shape[0] - 1
+    R_t = target.shape[0]
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.full((R_t,), -1, dtype=torch.int32, device=dev)
+    if out_len is None:
+        out_len = torch.zeros(B, dtype=torch.int32, device=dev)
+    if out_probs is None and want_probs:
+        out_probs = torch.empty((R_t, 2), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(B, R_t, dev)
+    st = lib.spec_verify(_ptr(target), _ptr(draft), _dtype(target), int(target.shape[1]), int(B),
+                         _ptr(draft_tokens), _ptr(cu_draft), _ptr(mode), _ptr(uniforms),
+                         float(temperature), _ptr(out_tokens), _ptr(out_len), _ptr(out_probs),
+                         _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("spec_verify", st)
+    return out_tokens, out_len, out_probs
+
+
+def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, cu_draft: torch.Tensor, *,
+                       out_tokens=None, out_len=None, workspace=None, stream=None):
+    """Strict (greedy) verify-and-commit. Returns (out_tokens, out_len)."""
+    lib = load()
+    B = cu_draft.shape[0] - 1
+    R_t = target.shape[0]
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.full((R_t,), -1, dtype=torch.int32, device=dev)
+    if out_len is None:
+        out_len = torch.zeros(B, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(B, R_t, dev)
+    st = lib.spec_verify_greedy(_ptr(target), _dtype(target), int(target.shape[1]), int(B),
+                                _ptr(draft_tokens), _ptr(cu_draft), _ptr(out_tokens), _ptr(out_len),
+                                _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("spec_verify_greedy", st)
+    return out_tokens, out_len
+
+
+def ngram_propose(histories: torch.Tensor, hist_len: torch.Tensor, min_n: int, max_n: int,
+                  max_tokens: int, *, out_tokens=None, out_count=None, out_n=None, stream=None):
+    """N-gram / prompt-lookup proposer. Returns (out_tokens [B, max_tokens], out_count, out_n)."""
+    lib = load()
+    B, stride = histories.shape
+    dev = histories.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, max_tokens), dtype=torch.int32, device=dev)
+    if out_count is None:
+        out_count = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_n is None:
+        out_n = torch.empty(B, dtype=torch.int32, device=dev)
+    st = lib.ngram_propose(_ptr(histories), int(stride), _ptr(hist_len), int(B), int(min_n),
+                           int(max_n), int(max_tokens), _ptr(out_tokens), _ptr(out_count),
+                           _ptr(out_n), _stream(stream))
+    _check("ngram_propose", st)
+    return out_tokens, out_count, out_n
+
+
+def sv_pack_drafts(tokens: torch.Tensor, counts: torch.Tensor, max_tokens: int, *, cu_draft=None,
+                   packed=None, stream=None):
+    """(cu_draft [B+1], packed [B*max_tokens]) from padded proposals and their counts."""
+    lib = load()
+    B = counts.shape[0]
+    dev = counts.device
+    if cu_draft is None:
+        cu_draft = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    if packed is None:
+        packed = torch.empty(max(B * max_tokens, 1), dtype=torch.int32, device=dev)
+    st = lib.sv_pack_drafts(_ptr(tokens), _ptr(counts), int(B), int(max_tokens), _ptr(cu_draft),
+                            _ptr(packed), _stream(stream))
+    _check("sv_pack_drafts", st)
+    return cu_draft, packed
+
+
+def sv_check_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronize, read and clear the device status word; returns the SV_DATA_* bits."""
+    bits = ctypes.c_uint32(0)
+    st = load().sv_check_status(_ptr(workspace), _stream(stream), ctypes.byref(bits))
+    if st not in (SV_OK, SV_ERR_DATA):
+        raise SpecVerifyError("sv_check_status", st)
+    return int(bits.value)

@@ -17,3 +17,18 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+TESTS = os.path.dirname(os.path.abspath(__file__))
+if TESTS not in sys.path:
+    sys.path.insert(0, TESTS)
+
+
+@pytest.fixture(scope="session")
+def cuda_lib():
+    """The CUDA library, built in-tree for sm_103a; GPU tests only."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_verification_27_gb300 import api, build
+    build.build_library()
+    return api.load()

@@ -1,0 +1,101 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports every
+function include/spec_verify.h declares, and rejects bad arguments on the host
+before touching CUDA."""
+import ctypes
+import subprocess
+
+import pytest
+
+from speculative_decoding_verification_27_gb300 import api, build
+
+FAKE = ctypes.c_void_p(0x10000)       # never dereferenced: validation rejects first
+MISALIGNED = ctypes.c_void_p(0x10001)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return api.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = api.header_functions()
+    assert {"spec_verify", "spec_verify_greedy", "ngram_propose", "sv_pack_drafts",
+            "sv_check_status", "sv_status_string", "spec_verify_workspace_size"} <= set(names)
+    exported = subprocess.run(["nm", "-D", "--defined-only", build.LIB_PATH], capture_output=True,
+                              text=True, check=True).stdout.split()
+    for n in names:
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_workspace_size(lib):
+    for B, R in [(1, 5), (64, 384), (256, 2048), (513, 3000)]:
+        assert api.spec_verify_workspace_size(B, R) == 64 + ((4 * B + 15) // 16) * 16 + 32 * R
+    assert lib.spec_verify_workspace_size(-1, 4) == 0
+
+
+def test_status_strings(lib):
+    assert api.status_string(0) == "SV_OK"
+    assert api.status_string(1) == "SV_ERR_INVALID_ARG"
+    assert api.status_string(5) == "SV_ERR_DATA"
+    assert api.status_string(99) == "SV_ERR_UNKNOWN"
+
+
+def _verify(lib, **kw):
+    a = dict(target=FAKE, draft=None, dtype=1, V=128, B=2, toks=FAKE, cu=FAKE, mode=None, u=FAKE,
+             T=1.0, ot=FAKE, ol=FAKE, op=None, ws=FAKE, wsb=1 << 20, st=None)
+    a.update(kw)
+    return lib.spec_verify(a["target"], a["draft"], a["dtype"], a["V"], a["B"], a["toks"], a["cu"],
+                           a["mode"], a["u"], a["T"], a["ot"], a["ol"], a["op"], a["ws"], a["wsb"],
+                           a["st"])
+
+
+def test_spec_verify_host_validation(lib):
+    E = api.SV_ERR_INVALID_ARG
+    assert _verify(lib, B=0) == api.SV_OK  # empty batch: nothing to do, nothing launched
+    assert _verify(lib, B=-1) == E
+    assert _verify(lib, V=0) == E
+    assert _verify(lib, V=1 << 20) == E        # beyond the largest vocabulary
+    assert _verify(lib, dtype=7) == E
+    assert _verify(lib, T=0.0) == E
+    assert _verify(lib, T=-1.0) == E
+    assert _verify(lib, T=float("nan")) == E
+    assert _verify(lib, T=float("inf")) == E
+    assert _verify(lib, target=None) == E
+    assert _verify(lib, cu=None) == E
+    assert _verify(lib, u=None) == E
+    assert _verify(lib, ot=None) == E
+    assert _verify(lib, ws=None) == E
+    assert _verify(lib, target=MISALIGNED) == E   # not element-aligned
+    assert _verify(lib, ws=MISALIGNED) == E
+    assert _verify(lib, wsb=16) == E               # smaller than the header
+    # Strict mode needs neither a temperature nor uniforms.
+    assert lib.spec_verify_greedy(FAKE, 1, 0, 2, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == E
+    assert lib.spec_verify_greedy(FAKE, 1, 16, 0, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == api.SV_OK
+
+
+def test_ngram_and_pack_host_validation(lib):
+    E = api.SV_ERR_INVALID_ARG
+    ng = lambda B=2, mn=1, mx=3, mt=5, stride=16: lib.ngram_propose(FAKE, stride, FAKE, B, mn, mx, mt, FAKE, FAKE, FAKE, None)
+    assert ng(B=0) == api.SV_OK
+    assert ng(B=-1) == E
+    assert ng(mn=0) == E
+    assert ng(mn=3, mx=2) == E
+    assert ng(mt=-1) == E
+    assert ng(stride=-1) == E
+    assert lib.ngram_propose(MISALIGNED, 16, FAKE, 2, 1, 3, 5, FAKE, FAKE, FAKE, None) == E
+    assert lib.sv_pack_drafts(FAKE, FAKE, -1, 5, FAKE, FAKE, None) == E
+    assert lib.sv_pack_drafts(FAKE, FAKE, 2, 5, None, FAKE, None) == E
+    bits = ctypes.c_uint32(0)
+    assert lib.sv_check_status(None, None, ctypes.byref(bits)) == E
+
+
+def test_python_binding_rejects_host_tensors(lib):
+    import torch
+    t = torch.zeros((3, 8), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        api.spec_verify_greedy(t, torch.zeros(2, dtype=torch.int32), torch.tensor([0, 2], dtype=torch.int32),
+                               out_tokens=torch.zeros(3, dtype=torch.int32),
+                               out_len=torch.zeros(1, dtype=torch.int32),
+                               workspace=torch.zeros(256, dtype=torch.uint8))

@@ -1,0 +1,218 @@
+"""GPU parity of spec_verify / spec_verify_greedy against the float64 oracle,
+through the C ABI, on the five benchmark configurations (full sizes where the
+oracle finishes in seconds) and on edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import parity
+from speculative_decoding_verification_27_gb300 import api
+from speculative_decoding_verification_27_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(batch, workspace=None):
+    db = parity.to_device(batch)
+    gpu = parity.gpu_verify(db, workspace)
+    ora = parity.oracle_verify(batch)
+    return parity.compare(batch, gpu, ora), gpu, ora
+
+
+# --------------------------------------------------------------------------
+# The five configurations
+# --------------------------------------------------------------------------
+def test_config1_sampling_1000_rounds(cuda_lib):
+    """B=1, K=4, V=32000 fp32, T=1: 1000 rounds of fresh logits, one workspace."""
+    ws = api.new_workspace(1, 5)
+    mism = flagged = rows = 0
+    for r in range(1000):
+        rep, _, _ = _run(W.config1(seed=101, round_index=r), ws)
+        mism += rep.mismatched_requests
+        flagged += rep.flagged_requests
+        rows += rep.rows
+    print(f"config1: rows={rows} flagged_requests={flagged} mismatched={mism}")
+    assert mism <= 1e-4 * rows
+    assert api.sv_check_status(ws) == 0
+
+
+def test_config2_greedy_full_bit_exact(cuda_lib):
+    b = W.config2(seed=102)
+    db = parity.to_device(b)
+    tok, ln = api.spec_verify_greedy(db.target, db.draft_tokens, db.cu_draft)
+    torch.cuda.synchronize()
+    ora = parity.oracle_verify(b)
+    tok, ln = tok.cpu().numpy(), ln.cpu().numpy()
+    assert np.array_equal(ln, ora.out_len)
+    t0 = b.cu_draft[:-1] + np.arange(b.B)
+    for i in range(b.B):
+        n = ln[i]
+        assert np.array_equal(tok[t0[i]:t0[i] + n], ora.out_tokens[t0[i]:t0[i] + n])
+    # The same through spec_verify with every request in GREEDY mode.
+    gpu = parity.gpu_verify(db)
+    rep = parity.compare(b, gpu, ora)
+    assert rep.mismatched_requests == 0 and rep.flagged_requests == 0
+
+
+def test_config3_sampling_full(cuda_lib):
+    """B=256, K=7, V=151936 bf16, T=0.7 (the benchmark's workload), every request."""
+    rep, _, _ = _run(W.config3(seed=103))
+    print("config3:", rep.as_dict())
+    assert rep.mismatched_requests <= 1e-4 * rep.rows
+
+
+def test_config3_literal_zipf_reading(cuda_lib):
+    rep, _, _ = _run(W.config3(seed=113, B=24, literal_zipf=True))
+    assert rep.mismatched_requests <= max(1, 1e-4 * rep.rows)
+
+
+def test_config4_ngram_then_one_hot_verify(cuda_lib):
+    import oracle
+    nb = W.config4_histories(seed=104)
+    h = torch.from_numpy(nb.histories).cuda()
+    hl = torch.from_numpy(nb.hist_len).cuda()
+    out, cnt, nn = api.ngram_propose(h, hl, nb.min_n, nb.max_n, nb.max_tokens)
+    cu, packed = api.sv_pack_drafts(out, cnt, nb.max_tokens)
+    torch.cuda.synchronize()
+    o_out, o_cnt, o_n = oracle.ngram_propose(nb.histories, nb.hist_len, nb.min_n, nb.max_n, nb.max_tokens)
+    assert np.array_equal(cnt.cpu().numpy(), o_cnt) and np.array_equal(nn.cpu().numpy(), o_n)
+    g_out = out.cpu().numpy()
+    for b in range(nb.histories.shape[0]):
+        assert np.array_equal(g_out[b, :o_cnt[b]], o_out[b, :o_cnt[b]])
+        assert np.all(g_out[b, o_cnt[b]:] == -1)
+    assert o_cnt.sum() > 0
+    vb = W.config4_verify(seed=104, proposals=o_out, counts=o_cnt)
+    assert np.array_equal(cu.cpu().numpy(), vb.cu_draft)
+    assert np.array_equal(packed.cpu().numpy()[:vb.R_d], vb.draft_tokens)
+    rep, _, _ = _run(vb)
+    assert rep.mismatched_requests <= max(1, 1e-4 * rep.rows)
+
+
+def test_config5_ragged_mixed_full(cuda_lib):
+    """B=512, K_b in 1..8, V=256000 bf16, half greedy requests."""
+    rep, _, _ = _run(W.config5(seed=105))
+    print("config5:", rep.as_dict())
+    assert rep.mismatched_requests <= max(1, 1e-4 * rep.rows)
+
+
+# --------------------------------------------------------------------------
+# Edge cases
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("V", [1, 2, 3, 7, 33, 1000, 4097, 8200])
+def test_small_and_ragged_vocab(cuda_lib, dtype, V):
+    """V not a multiple of the vector width takes the scalar-load path."""
+    Ks = np.array([0, 1, 3, 5, 2, 0, 4], np.int32)
+    b = W.gaussian_sampling(seed=200 + V, B=Ks.size, K=Ks, V=V, sigma=2.0, draft_sigma=0.7,
+                            T=0.9, dtype=dtype)
+    b.mode = np.array([0, 1, 0, 0, 1, 0, 0], np.uint8)
+    rep, _, _ = _run(b)
+    assert rep.mismatched_requests <= 1
+
+
+@pytest.mark.parametrize("T", [0.3, 1.0, 2.5])
+def test_temperatures(cuda_lib, T):
+    b = W.gaussian_sampling(seed=300, B=40, K=5, V=5000, sigma=3.0, draft_sigma=1.0, T=T, dtype="bf16")
+    rep, _, _ = _run(b)
+    assert rep.mismatched_requests <= 1
+
+
+def test_one_hot_proposals(cuda_lib):
+    b = W.gaussian_sampling(seed=301, B=64, K=4, V=3000, sigma=1.0, draft_sigma=0.5, T=1.0)
+    b.draft = None
+    rep, _, _ = _run(b)
+    assert rep.mismatched_requests <= 1
+
+
+def test_unaligned_rows_take_scalar_path(cuda_lib):
+    """Logit base pointer not 16-byte aligned (element aligned only)."""
+    b = W.gaussian_sampling(seed=302, B=16, K=3, V=4096, sigma=2.0, draft_sigma=0.5, T=1.0, dtype="bf16")
+    db = parity.to_device(b)
+    flat = torch.empty(db.target.numel() + 1, dtype=torch.bfloat16, device="cuda")
+    flat[1:].copy_(db.target.reshape(-1))
+    db.target = flat[1:].view(db.target.shape)
+    assert db.target.data_ptr() % 16 != 0
+    gpu = parity.gpu_verify(db)
+    parity.compare(b, gpu, parity.oracle_verify(b))
+
+
+def test_masked_logits_and_ties(cuda_lib):
+    V = 64
+    zt = np.full((6, V), -np.inf, np.float32)
+    zt[:, 5] = 1.0
+    zt[:, 9] = 1.0   # tie with 5: greedy argmax is 5
+    zt[:, 40] = 0.5
+    zd = np.full((4, V), -np.inf, np.float32)
+    zd[:, 9] = 0.0
+    zd[:, 40] = 0.0
+    cu = np.array([0, 2, 4], np.int32)
+    toks = np.array([9, 40, 5, 9], np.int32)
+    for mode in (np.array([0, 1], np.uint8), np.array([1, 0], np.uint8)):
+        b = W.VerifyBatch("masked", zt, zd, toks, cu, W.uniforms_for(cu, 7), 1.0, mode)
+        rep, gpu, ora = _run(b)
+        assert rep.mismatched_requests == 0
+
+
+def test_empty_batch_is_a_noop(cuda_lib):
+    z = torch.zeros((1, 8), device="cuda")
+    cu = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tok, ln, _ = api.spec_verify(z, None, torch.zeros(1, dtype=torch.int32, device="cuda"), cu,
+                                 torch.zeros((1, 2), device="cuda"), 1.0)
+    torch.cuda.synchronize()
+    assert ln.numel() == 0
+
+
+def test_rerun_is_bit_identical(cuda_lib):
+    b = W.config5(seed=303, B=48, V=20000)
+    db = parity.to_device(b)
+    a = parity.gpu_verify(db)
+    c = parity.gpu_verify(db)
+    for x, y in zip(a, c):
+        assert np.array_equal(x, y)
+
+
+def test_data_errors_set_status_and_leave_workspace_usable(cuda_lib):
+    b = W.gaussian_sampling(seed=304, B=8, K=3, V=512, sigma=1.0, draft_sigma=0.5, T=1.0)
+    ws = api.new_workspace(b.B, b.R_t)
+    db = parity.to_device(b)
+    bad = db.draft_tokens.clone()
+    bad[2] = 512  # out of range
+    api.spec_verify(db.target, db.draft, bad, db.cu_draft, db.uniforms, 1.0, workspace=ws)
+    assert api.sv_check_status(ws) & api.SV_DATA_BAD_TOKEN
+    cu_bad = db.cu_draft.clone()
+    cu_bad[3] = 1  # decreasing offsets
+    api.spec_verify(db.target, db.draft, db.draft_tokens, cu_bad, db.uniforms, 1.0, workspace=ws)
+    assert api.sv_check_status(ws) & api.SV_DATA_BAD_OFFSETS
+    gpu = parity.gpu_verify(db, ws)
+    parity.compare(b, gpu, parity.oracle_verify(b))
+    assert api.sv_check_status(ws) == 0
+
+
+# --------------------------------------------------------------------------
+# Statistics of the GPU path itself
+# --------------------------------------------------------------------------
+def test_chi_square_through_the_gpu(cuda_lib):
+    """1e6 rounds, V=16, K=1: the first emitted token follows p (lossless)."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(12)
+    V, N = 16, 1_000_000
+    zp = rng.normal(0, 1.5, V).astype(np.float32)
+    zb = rng.normal(0, 1.5, V).astype(np.float32)
+    zq = (zp + rng.normal(0, 1.0, V)).astype(np.float32)
+    p = softmax(zp.astype(np.float64))
+    q = softmax(zq.astype(np.float64))
+    cu = np.arange(N + 1, dtype=np.int32)
+    toks = np.searchsorted(np.cumsum(q), rng.random(N), side="right").clip(0, V - 1).astype(np.int32)
+    target = torch.from_numpy(np.stack([zp, zb])).cuda().repeat(N, 1)
+    draft = torch.from_numpy(zq[None]).cuda().repeat(N, 1)
+    tok, ln, _ = api.spec_verify(target, draft, torch.from_numpy(toks).cuda(),
+                                 torch.from_numpy(cu).cuda(),
+                                 torch.from_numpy(W.uniforms_for(cu, seed=21)).cuda(), 1.0,
+                                 want_probs=False)
+    first = tok.view(N, 2)[:, 0].cpu().numpy()
+    hist = np.bincount(first, minlength=V)
+    chi2 = float(((hist - N * p) ** 2 / (N * p)).sum())
+    assert chi2 < 37.70, chi2
+    alpha = np.minimum(p, q).sum()
+    acc = (ln.cpu().numpy() == 2).mean()
+    assert abs(acc - alpha) < 5 * np.sqrt(alpha * (1 - alpha) / N)
