@@ -121,12 +121,13 @@ class VerifyResult:
 
 
 def spec_verify(target, draft, draft_tokens, cu_draft, uniforms, temperature: float,
-                mode=None, nthreads: int = 0) -> VerifyResult:
+                mode=None, nthreads: int = 0, diagnostics: bool = True) -> VerifyResult:
     """Verify-and-commit for a packed batch (layout as the CUDA library's).
 
     target: [R_t, V] float32 or uint16(bf16); draft: [R_d, V] same dtype or None
     (one-hot q); draft_tokens: [R_d] int32; cu_draft: [B+1] int32; uniforms:
-    [R_t, 2] float32; mode: [B] uint8 (0 sample, 1 greedy) or None.
+    [R_t, 2] float32; mode: [B] uint8 (0 sample, 1 greedy) or None. diagnostics=False skips the
+    per-row (p(x̂), q(x̂)) outputs, leaving only the method's own work.
     """
     target, dt = _logits(target)
     V = target.shape[-1]
@@ -149,8 +150,8 @@ def spec_verify(target, draft, draft_tokens, cu_draft, uniforms, temperature: fl
     stop = np.zeros(B, np.int32)
     st = _load().oracle_spec_verify(
         _ptr(target), _ptr(draft), dt, V, B, _ptr(draft_tokens), _ptr(cu_draft), _ptr(mode),
-        _ptr(uniforms), float(temperature), _ptr(out_tokens), _ptr(out_len), _ptr(out_probs),
-        _ptr(margin), _ptr(rho), _ptr(stop), int(nthreads))
+        _ptr(uniforms), float(temperature), _ptr(out_tokens), _ptr(out_len),
+        _ptr(out_probs) if diagnostics else None, _ptr(margin), _ptr(rho), _ptr(stop), int(nthreads))
     if st != 0:
         raise ValueError(f"oracle_spec_verify: invalid request data (code {st})")
     return VerifyResult(out_tokens, out_len, out_probs, margin, rho, stop)

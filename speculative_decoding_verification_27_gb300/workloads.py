@@ -9,7 +9,8 @@ arithmetic: no softmax, no accept test, no residual, no inverse-CDF draw.
   definition: key = the 64-bit seed, counter = (request b, slot i, round, 0);
   word 0 gives the accept uniform u, word 1 the draw uniform u', each as
   (w >> 8) * 2**-24, so every uniform is an exact float32 in [0, 1).
-* Logit noise comes from numpy's PCG64 generator seeded from (seed, stream).
+* Logit noise comes from torch's seeded CPU generator; permutations, choices
+  and Gumbel uniforms from numpy's PCG64, both seeded from (seed, stream).
 * Draft tokens "sampled from q" use the Gumbel-max identity:
   argmax_x (z_x / T + G_x), G_x = -log(-log U_x), is an exact sample of
   softmax(z / T) without computing that softmax.
@@ -97,12 +98,13 @@ def uniforms_for(cu_draft: np.ndarray, seed: int, round_index: int = 0) -> np.nd
 # ----------------------------------------------------------------------------
 # bf16 storage
 # ----------------------------------------------------------------------------
-def to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float32 to bf16 (nearest-even) and return the 16-bit patterns."""
-    x = np.ascontiguousarray(x, np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    u = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
-    return u.astype(np.uint16)
+def to_bf16_bits(x) -> np.ndarray:
+    """Round float32 to bf16 (nearest-even) and return the 16-bit patterns
+    (torch's conversion, multi-threaded; checked bit for bit against the
+    round-to-nearest-even formula in the tests)."""
+    import torch
+    t = x if isinstance(x, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(x, np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -186,15 +188,32 @@ def _rng(seed: int, *stream: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(seed) & 0xFFFFFFFF, *stream])))
 
 
+class _Normal:
+    """Seeded float32 Gaussian noise from torch's CPU generator (multi-threaded;
+    numpy's sampler is several times slower at these sizes)."""
+
+    def __init__(self, rng: np.random.Generator):
+        import torch
+        self._torch = torch
+        self._g = torch.Generator().manual_seed(int(rng.integers(0, 2 ** 62)))
+
+    def __call__(self, shape, sigma: float = 1.0) -> np.ndarray:
+        z = self._torch.randn(shape, generator=self._g, dtype=self._torch.float32)
+        if sigma != 1.0:
+            z.mul_(float(sigma))
+        return z.numpy()
+
+
 def _gumbel_argmax(z: np.ndarray, T: float, rng: np.random.Generator, chunk: int = 64) -> np.ndarray:
-    """x̂ ~ softmax(z / T) per row via argmax(z / T + Gumbel noise)."""
+    """x̂ ~ softmax(z / T) per row via argmax(z / T + Gumbel noise), float64."""
+    import torch
+    g = torch.Generator().manual_seed(int(rng.integers(0, 2 ** 62)))
     out = np.empty(z.shape[0], np.int32)
     for r0 in range(0, z.shape[0], chunk):
-        zz = logits_as_f32(z[r0:r0 + chunk]).astype(np.float64) / T
-        u = rng.random(zz.shape)
-        np.maximum(u, 1e-300, out=u)
-        g = -np.log(-np.log(u))
-        out[r0:r0 + chunk] = np.argmax(zz + g, axis=1)
+        zz = torch.from_numpy(logits_as_f32(z[r0:r0 + chunk])).double().div_(T)
+        u = torch.rand(zz.shape, generator=g, dtype=torch.float64).clamp_(min=1e-300)
+        zz.sub_(u.log_().neg_().log_())
+        out[r0:r0 + chunk] = zz.argmax(dim=1).numpy()
     return out
 
 
@@ -227,14 +246,15 @@ def gaussian_sampling(seed: int, B: int, K, V: int, sigma: float, draft_sigma: f
                       name: str = "gaussian") -> VerifyBatch:
     """Sampling batch with z_t ~ N(0, sigma^2), z_d = z_t + N(0, draft_sigma^2), x̂ ~ q."""
     rng = _rng(seed, 1, round_index)
+    normal = _Normal(rng)
     Ks = np.full(B, K, np.int32) if np.isscalar(K) else np.asarray(K, np.int32)
     cu = _ragged_cu(Ks)
     R_t, R_d = int(cu[-1]) + B, int(cu[-1])
-    zt = rng.standard_normal((R_t, V), dtype=np.float32) * np.float32(sigma)
+    zt = normal((R_t, V), sigma)
     if dtype == "bf16":
         zt = bf16_bits_to_f32(to_bf16_bits(zt))
     rows = _target_rows_of_draft_slots(cu)
-    zd = zt[rows] + rng.standard_normal((R_d, V), dtype=np.float32) * np.float32(draft_sigma)
+    zd = zt[rows] + normal((R_d, V), draft_sigma)
     if dtype == "bf16":
         zt_s, zd_s = to_bf16_bits(zt), to_bf16_bits(zd)
     else:
@@ -255,7 +275,7 @@ def config2(seed: int = 2, B: int = 64, K: int = 5, V: int = 128256,
     rng = _rng(seed, 2)
     cu = _ragged_cu(np.full(B, K, np.int32))
     R_t = int(cu[-1]) + B
-    z = bf16_bits_to_f32(to_bf16_bits(rng.standard_normal((R_t, V), dtype=np.float32) * np.float32(3.0)))
+    z = bf16_bits_to_f32(to_bf16_bits(_Normal(rng)((R_t, V), 3.0)))
     win = rng.integers(0, V, R_t)
     others = z.copy()
     others[np.arange(R_t), win] = -np.inf
@@ -284,18 +304,24 @@ def config3(seed: int = 3, B: int = 256, K: int = 7, V: int = 151936, T: float =
     R_t, R_d = int(cu[-1]) + B, int(cu[-1])
     r = np.arange(1, V + 1, dtype=np.float64)
     base = (zipf_scale * r ** -zipf_s if literal_zipf else -zipf_scale * zipf_s * np.log(r)).astype(np.float32)
+    import torch
+    base_t = torch.from_numpy(base)
+    normal = _Normal(rng)
     zt = np.empty((R_t, V), np.uint16)
     chunk = 128
     for r0 in range(0, R_t, chunk):
         n = min(chunk, R_t - r0)
-        perm = rng.permuted(np.broadcast_to(np.arange(V, dtype=np.int32), (n, V)), axis=1)
-        zt[r0:r0 + n] = to_bf16_bits(base[perm] + rng.standard_normal((n, V), dtype=np.float32))
+        # z[j] = base[sigma(j)] for a uniformly random permutation sigma of the
+        # ranks (sigma is the inverse of pi, and is itself uniform).
+        sig = np.empty((n, V), np.int64)
+        for k in range(n):
+            sig[k] = rng.permutation(V)
+        zt[r0:r0 + n] = to_bf16_bits(base_t[torch.from_numpy(sig)].add_(torch.from_numpy(normal((n, V)))))
     rows = _target_rows_of_draft_slots(cu)
     zd = np.empty((R_d, V), np.uint16)
     for r0 in range(0, R_d, chunk):
         n = min(chunk, R_d - r0)
-        zd[r0:r0 + n] = to_bf16_bits(bf16_bits_to_f32(zt[rows[r0:r0 + n]]) +
-                                     rng.standard_normal((n, V), dtype=np.float32))
+        zd[r0:r0 + n] = to_bf16_bits(bf16_bits_to_f32(zt[rows[r0:r0 + n]]) + normal((n, V)))
     toks = _gumbel_argmax(zd, T, rng)
     return VerifyBatch("config3", zt, zd, toks, cu, uniforms_for(cu, seed), T, None,
                        {"seed": seed, "literal_zipf": literal_zipf})
@@ -317,10 +343,14 @@ def config4_histories(seed: int = 4, B: int = 128, L: int = 8192, V: int = 32000
             continue
         while covered.sum() < coverage * Lb:
             ln = int(rng.integers(span[0], min(span[1], Lb // 2) + 1))
-            d = int(rng.integers(ln, Lb - ln + 1))
+            # Destinations start anywhere after one span length and are clipped
+            # at the end, so every position (the tail included) is equally
+            # likely to lie in a copy; the source lies wholly before it.
+            d = int(rng.integers(ln, Lb))
+            m = min(ln, Lb - d)
             s = int(rng.integers(0, d - ln + 1))
-            h[b, d:d + ln] = h[b, s:s + ln]
-            covered[d:d + ln] = True
+            h[b, d:d + m] = h[b, s:s + m]
+            covered[d:d + m] = True
     return NgramBatch(h, lens, n, n, max_tokens)
 
 
@@ -334,7 +364,7 @@ def config4_verify(seed: int, proposals: np.ndarray, counts: np.ndarray, V: int 
     R_t = int(cu[-1]) + B
     toks = np.concatenate([proposals[b, :counts[b]] for b in range(B)]).astype(np.int32) \
         if int(cu[-1]) else np.zeros(0, np.int32)
-    zt = rng.standard_normal((R_t, V), dtype=np.float32) * np.float32(sigma)
+    zt = _Normal(rng)((R_t, V), sigma)
     return VerifyBatch("config4", zt, None, toks, cu, uniforms_for(cu, seed), 1.0, None,
                        {"seed": seed})
 
@@ -347,11 +377,12 @@ def config5(seed: int = 5, B: int = 512, V: int = 256000, Kmax: int = 8, T: floa
     mode = (rng.random(B) < p_greedy).astype(np.uint8)
     cu = _ragged_cu(Ks)
     R_t, R_d = int(cu[-1]) + B, int(cu[-1])
+    normal = _Normal(rng)
     zt = np.empty((R_t, V), np.uint16)
     chunk = 128
     for r0 in range(0, R_t, chunk):
         n = min(chunk, R_t - r0)
-        zt[r0:r0 + n] = to_bf16_bits(rng.standard_normal((n, V), dtype=np.float32) * np.float32(sigma))
+        zt[r0:r0 + n] = to_bf16_bits(normal((n, V), sigma))
     rows = _target_rows_of_draft_slots(cu)
     req_of_slot = np.repeat(np.arange(B), Ks)
     samp_slots = np.nonzero(mode[req_of_slot] == 0)[0]
@@ -359,8 +390,7 @@ def config5(seed: int = 5, B: int = 512, V: int = 256000, Kmax: int = 8, T: floa
     zd = np.zeros((R_d, V), np.uint16)
     for s0 in range(0, samp_slots.shape[0], chunk):
         sl = samp_slots[s0:s0 + chunk]
-        zd[sl] = to_bf16_bits(bf16_bits_to_f32(zt[rows[sl]]) +
-                              rng.standard_normal((sl.shape[0], V), dtype=np.float32) * np.float32(draft_sigma))
+        zd[sl] = to_bf16_bits(bf16_bits_to_f32(zt[rows[sl]]) + normal((sl.shape[0], V), draft_sigma))
     toks = np.zeros(R_d, np.int32)
     if samp_slots.size:
         toks[samp_slots] = _gumbel_argmax(zd[samp_slots], T, rng)

@@ -36,13 +36,19 @@ def test_uniforms_exact_and_layout_independent():
     assert not np.array_equal(W.uniforms_for(cu, 98), u)
 
 
-def test_bf16_rounding_matches_torch():
+def test_bf16_rounding_is_nearest_even():
     rng = np.random.default_rng(1)
-    x = np.concatenate([rng.normal(0, 10, 100000), [0.0, -0.0, 1e-40, 3.0e38, -7.5]]).astype(np.float32)
+    x = np.concatenate([rng.normal(0, 10, 100000), [0.0, -0.0, 1e-40, 3.0e38, -7.5, -np.inf, np.inf],
+                        # exact halfway cases: ties go to the even 16-bit pattern
+                        np.array([0x3F808000, 0x3F818000, 0xBF808000], np.uint32).view(np.float32)]
+                       ).astype(np.float32)
     ours = W.to_bf16_bits(x)
-    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    u = x.view(np.uint32).astype(np.uint64)
+    ref = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
     assert np.array_equal(ours, ref)
-    assert np.array_equal(W.bf16_bits_to_f32(ours), torch.from_numpy(x).to(torch.bfloat16).float().numpy())
+    assert list(ours[-3:]) == [0x3F80, 0x3F82, 0xBF80]
+    f = W.bf16_bits_to_f32(ours)
+    assert np.all(np.abs(f[:100000] - x[:100000]) <= np.abs(x[:100000]) * 2.0 ** -8)
 
 
 def test_gumbel_draft_tokens_follow_q():
