@@ -216,7 +216,7 @@ def run_ours(args):
     batch = make_batch(args.seed + rank, args.batch)
     db = parity.to_device(batch)
     B, R_t = batch.B, batch.R_t
-    ws = api.new_workspace(B, R_t)
+    ws = api.new_workspace(B, R_t, batch.V)
     out_tokens = torch.full((R_t,), -1, dtype=torch.int32, device="cuda")
     out_len = torch.zeros(B, dtype=torch.int32, device="cuda")
     out_probs = torch.empty((R_t, 2), dtype=torch.float32, device="cuda")

@@ -65,7 +65,7 @@ typedef enum {
   SV_OK = 0,
   SV_ERR_INVALID_ARG = 1,   /* rejected on the host before any launch */
   SV_ERR_CUDA = 2,          /* a CUDA runtime call or launch failed */
-  SV_ERR_TIMEOUT = 3,       /* reserved: a bounded device-side wait gave up */
+  SV_ERR_TIMEOUT = 3,       /* a bounded device-side wait gave up (sv_check_status) */
   SV_ERR_UNIMPLEMENTED = 4, /* reserved */
   SV_ERR_DATA = 5           /* sv_check_status found device-side data errors */
 } sv_status;
@@ -80,15 +80,22 @@ enum { SV_MODE_SAMPLE = 0, SV_MODE_GREEDY = 1 };
 #define SV_DATA_EMPTY_ROW 0x4u     /* a sampled row without any finite logit */
 #define SV_DATA_BAD_MODE 0x8u      /* mode[b] not SAMPLE or GREEDY (treated as SAMPLE) */
 #define SV_DATA_DEGENERATE_RESIDUAL 0x10u /* informational: residual mass 0 after a reject; drew from p */
+#define SV_DEV_COPY_TIMEOUT 0x20u  /* a bounded wait for an asynchronous copy gave up (never expected);
+                                      the call's outputs are invalid and the workspace must be
+                                      zero-filled again before reuse */
 
 /*
- * Bytes of workspace spec_verify / spec_verify_greedy need for B requests
- * and R_t target rows. The workspace must be 16-byte aligned and zero-filled
+ * Bytes of workspace spec_verify / spec_verify_greedy need for B requests,
+ * R_t target rows and vocabulary size V (0 if an argument is out of range).
+ * The workspace holds a 64-byte header, one counter per request, a 32-byte
+ * record per target row and, for up to min(B, 4096) final draws that the
+ * kernel splits across CTAs near the end of a call, a descriptor and the
+ * partial sums of each. It must be 16-byte aligned and zero-filled
  * before its first use; every call leaves its counters at zero again, so
  * calls in stream order may reuse it without clearing. Calls that may run
  * concurrently (other streams) need distinct workspaces.
  */
-size_t spec_verify_workspace_size(int32_t B, int32_t R_t);
+size_t spec_verify_workspace_size(int32_t B, int32_t R_t, int32_t V);
 
 /*
  * Lossless verify-and-commit ("Draft Model（草稿模型）", §2 and the algorithm
@@ -99,7 +106,7 @@ size_t spec_verify_workspace_size(int32_t B, int32_t R_t);
  *                  (q = e_x̂, "5.2 Draft 模型与无模型方案" §4.3); then
  *                  min(1, p/q) = p(x̂) and the residual is p without x̂.
  *   dtype          SV_FP32 or SV_BF16 for both logit matrices.
- *   V >= 1, B >= 0 (B == 0 is a no-op).
+ *   1 <= V <= 262144 (fp32) or 524288 (bf16); B >= 0 (B == 0 is a no-op).
  *   draft_tokens   [R_d] int32 proposed tokens (may be NULL when R_d == 0).
  *   cu_draft       [B+1] int32 offsets (see the layout above).
  *   mode           [B] uint8 SV_MODE_* per request, or NULL (all SAMPLE).
@@ -118,7 +125,7 @@ size_t spec_verify_workspace_size(int32_t B, int32_t R_t);
  *                  the bonus-slot row K_b gets (p_s(y), q_s(y)) of the final
  *                  token y drawn at the stop row s (q_s(y) = 0 for a bonus
  *                  draw). GREEDY requests get (-1, -1).
- *   workspace      device scratch, >= spec_verify_workspace_size(B, R_t)
+ *   workspace      device scratch, >= spec_verify_workspace_size(B, R_t, V)
  *                  bytes, 16-byte aligned, zero-filled before first use.
  *
  * Decision rule: accept slot i iff u_i < min(1, p(x̂_i)/q(x̂_i)), with
@@ -179,9 +186,10 @@ sv_status sv_pack_drafts(const int32_t* tokens, const int32_t* counts, int32_t B
 
 /*
  * Synchronizes `cuda_stream`, reads the status word of `workspace` into
- * *out_bits (SV_DATA_* bits) and clears it. Returns SV_OK when no error bit
- * is set (SV_DATA_DEGENERATE_RESIDUAL alone is informational), SV_ERR_DATA
- * otherwise, or SV_ERR_CUDA / SV_ERR_INVALID_ARG.
+ * *out_bits (SV_DATA_* / SV_DEV_* bits) and clears it. Returns SV_OK when no
+ * error bit is set (SV_DATA_DEGENERATE_RESIDUAL alone is informational),
+ * SV_ERR_TIMEOUT if SV_DEV_COPY_TIMEOUT is set, SV_ERR_DATA for other bits,
+ * or SV_ERR_CUDA / SV_ERR_INVALID_ARG.
  */
 sv_status sv_check_status(void* workspace, void* cuda_stream, uint32_t* out_bits);
 

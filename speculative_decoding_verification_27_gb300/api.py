@@ -23,6 +23,7 @@ SV_DATA_BAD_TOKEN = 0x2
 SV_DATA_EMPTY_ROW = 0x4
 SV_DATA_BAD_MODE = 0x8
 SV_DATA_DEGENERATE_RESIDUAL = 0x10
+SV_DEV_COPY_TIMEOUT = 0x20
 
 HEADER = os.path.join(ROOT, "include", "spec_verify.h")
 
@@ -46,7 +47,7 @@ def load() -> ctypes.CDLL:
             "(speculative_decoding_verification_27_gb300.build.build_library())")
     lib = ctypes.CDLL(LIB_PATH)
     P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
-    lib.spec_verify_workspace_size.argtypes = [i32, i32]
+    lib.spec_verify_workspace_size.argtypes = [i32, i32, i32]
     lib.spec_verify_workspace_size.restype = sz
     lib.spec_verify.argtypes = [P, P, ctypes.c_int, i32, i32, P, P, P, P, f32, P, P, P, P, sz, P]
     lib.spec_verify.restype = ctypes.c_int
@@ -103,13 +104,13 @@ def _dtype(t: torch.Tensor) -> int:
     raise ValueError("logits must be float32 or bfloat16")
 
 
-def spec_verify_workspace_size(B: int, R_t: int) -> int:
-    return int(load().spec_verify_workspace_size(int(B), int(R_t)))
+def spec_verify_workspace_size(B: int, R_t: int, V: int) -> int:
+    return int(load().spec_verify_workspace_size(int(B), int(R_t), int(V)))
 
 
-def new_workspace(B: int, R_t: int, device="cuda") -> torch.Tensor:
+def new_workspace(B: int, R_t: int, V: int, device="cuda") -> torch.Tensor:
     """Zero-filled workspace (the library leaves it zeroed after each call)."""
-    return torch.zeros(spec_verify_workspace_size(B, R_t), dtype=torch.uint8, device=device)
+    return torch.zeros(spec_verify_workspace_size(B, R_t, V), dtype=torch.uint8, device=device)
 
 
 def spec_verify(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor,
@@ -128,7 +129,7 @@ def spec_verify(target: torch.Tensor, draft: Optional[torch.Tensor], draft_token
     if out_probs is None and want_probs:
         out_probs = torch.empty((R_t, 2), dtype=torch.float32, device=dev)
     if workspace is None:
-        workspace = new_workspace(B, R_t, dev)
+        workspace = new_workspace(B, R_t, target.shape[1], dev)
     st = lib.spec_verify(_ptr(target), _ptr(draft), _dtype(target), int(target.shape[1]), int(B),
                          _ptr(draft_tokens), _ptr(cu_draft), _ptr(mode), _ptr(uniforms),
                          float(temperature), _ptr(out_tokens), _ptr(out_len), _ptr(out_probs),
@@ -149,7 +150,7 @@ def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, cu_draf
     if out_len is None:
         out_len = torch.zeros(B, dtype=torch.int32, device=dev)
     if workspace is None:
-        workspace = new_workspace(B, R_t, dev)
+        workspace = new_workspace(B, R_t, target.shape[1], dev)
     st = lib.spec_verify_greedy(_ptr(target), _dtype(target), int(target.shape[1]), int(B),
                                 _ptr(draft_tokens), _ptr(cu_draft), _ptr(out_tokens), _ptr(out_len),
                                 _ptr(workspace), workspace.numel(), _stream(stream))
@@ -196,6 +197,6 @@ def sv_check_status(workspace: torch.Tensor, stream=None) -> int:
     """Synchronize, read and clear the device status word; returns the SV_DATA_* bits."""
     bits = ctypes.c_uint32(0)
     st = load().sv_check_status(_ptr(workspace), _stream(stream), ctypes.byref(bits))
-    if st not in (SV_OK, SV_ERR_DATA):
+    if st not in (SV_OK, SV_ERR_DATA, SV_ERR_TIMEOUT):
         raise SpecVerifyError("sv_check_status", st)
     return int(bits.value)

@@ -4,15 +4,17 @@
 //
 //   1. Row pass. Work items are target rows t = (request b, slot i), handed
 //      out in request order by an atomic counter. The CTA streams the target
-//      row (and, for a sampled draft slot, the paired draft row) once with
-//      16-byte loads and keeps a single-pass online softmax: per thread a
-//      running maximum and one fp32 partial sum per vector lane, rescaled when
-//      the maximum grows. Sums are combined in double-float arithmetic, so
+//      row (and, for a sampled draft slot, the paired draft row) once through
+//      a ring of shared-memory stages filled by bulk asynchronous copies (the
+//      TMA engine), with bulk L2 prefetches running a few chunks ahead of the
+//      ring, and keeps a single-pass online softmax: per thread a running
+//      maximum and one fp32 partial sum per vector lane, rescaled when the
+//      maximum grows. Sums are combined in double-float arithmetic, so
 //      S = sum_x 2^(z_x c - Mc) (c = log2(e)/T, Mc = fp32(max z * c)) is
 //      accurate to ~1e-9 relative. Greedy rows compute the argmax instead
 //      (lowest index among ties). The CTA then gathers z[x̂] and decides the
-//      slot: accept iff u < min(1, p(x̂)/q(x̂)) ("Draft Model（草稿模型）",
-//      §2 "接受-拒绝准则"; a zero draft probability rejects, "投机解码从零实现"
+//      slot: accept iff u < min(1, p(x̂)/q(x̂)) ("Draft Model（草稿模型）", §2
+//      "接受-拒绝准则"; a zero draft probability rejects, "投机解码从零实现"
 //      §4.3), or, strict mode, iff x̂ == argmax ("Speculative Decoding在分布式
 //      推理中的应用", §二). The per-row record goes to the workspace.
 //   2. Commit. Each finished row bumps its request's counter; the CTA that
@@ -24,11 +26,14 @@
 //        all accepted       r = p                  (bonus token, algorithm box)
 //        greedy request     the argmax of row s
 //      The draw is the inverse CDF in vocabulary order: the smallest k whose
-//      running sum of r exceeds u' * sum(r). It re-reads the stop row pair
-//      (usually still in L2): pass A computes per-warp sums of r for every
-//      tile, pass B rescans only the tile that holds the target.
+//      running sum of r exceeds u' * sum(r). The stop row (pair) is
+//      prefetched into L2 whole, then streamed through the ring once to sum
+//      r over every tile; only the tile that holds the target is rescanned.
 //   The last CTA to leave resets the work counter, and each request's counter
 //   is reset by its commit, so the workspace is left zeroed.
+//
+// Rows whose base is not 16-byte aligned (or whose byte length is not a
+// multiple of 16) take the same steps with scalar global loads.
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -40,9 +45,12 @@ namespace sv {
 
 struct WsHeader {
   unsigned int status;     // SV_DATA_* bits (sticky until sv_check_status)
-  unsigned int next_item;  // work counter of the persistent kernel
+  unsigned int next_item;  // next row to hand out
   unsigned int exited;     // CTAs that left the work loop
-  unsigned int pad[13];
+  unsigned int n_draws;    // draw slots reserved
+  unsigned int draw_head;  // slots before this one are fully handed out
+  unsigned int committed;  // requests committed
+  unsigned int pad[10];
 };
 static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
 
@@ -57,11 +65,65 @@ struct alignas(16) RowRec {
 };
 static_assert(sizeof(RowRec) == 32, "row record is 32 bytes");
 
+// A draw published in parts (64 bytes); `done` counts finished parts. The
+// slot's state word packs the part count (bits 20..31, 0 = not published)
+// and the parts handed out (bits 0..19), so one load checks a slot and one
+// atomic claims a part.
+constexpr unsigned kSlotCountBits = 20;
+constexpr unsigned kSlotCountMask = (1u << kSlotCountBits) - 1u;
+struct alignas(16) DrawDesc {
+  int b;            // request
+  int row;          // stop row (target row index)
+  int drow;         // paired draft row index, or -1
+  int kind;         // DrawKind
+  int xhat;         // the rejected one-hot proposal, or -1
+  float mcp, mcq;   // exponent offsets of the stop rows
+  int nparts;       // parts the draw is split into
+  double Sp, Sq;    // sums of the stop rows
+  unsigned unused;
+  unsigned done;    // parts finished
+  int bonus_row;    // row that receives (p(y), q(y)) of the drawn token
+  int pad;
+};
+static_assert(sizeof(DrawDesc) == 64, "draw descriptor is 64 bytes");
+
 constexpr int kMaxScanTiles = kThreads;   // the draw scans at most one tile per thread
 // Largest vocabulary for each element type: kMaxScanTiles tiles of one
 // 16-byte vector per thread (fp32 262144, bf16 524288).
 constexpr int max_vocab(int dtype) { return kMaxScanTiles * kThreads * (dtype == 0 ? 4 : 8); }
-constexpr int kScanUnroll = 4;            // tiles loaded ahead in the draw passes
+
+// Shared-memory ring of the bulk-copy streams.
+#ifndef SV_STAGES
+#define SV_STAGES 2
+#endif
+#ifndef SV_VPT
+#define SV_VPT 4
+#endif
+#ifndef SV_MINBLOCKS
+#define SV_MINBLOCKS 3
+#endif
+#ifndef SV_PART_CHUNKS
+#define SV_PART_CHUNKS 2
+#endif
+#ifndef SV_PUBLISH_WAVES
+#define SV_PUBLISH_WAVES 0
+#endif
+constexpr int kStages = SV_STAGES;                  // stages (kStages - 1 in flight)
+constexpr int kVPT = SV_VPT;                        // 16-byte vectors per thread per chunk
+constexpr int kChunkBytes = kThreads * 16 * kVPT;   // bytes of one row per stage
+constexpr int kStageBytes = 2 * kChunkBytes;        // target + draft chunk
+constexpr int kRingBytes = kStages * kStageBytes;   // dynamic shared memory per CTA
+constexpr int kPartChunks = SV_PART_CHUNKS;         // ring chunks per draw part
+constexpr int kMaxParts = 16;                       // parts a draw is split into, at most
+constexpr int kMaxDrawSlots = 4096;                 // draws that can be published per call
+// Draws are split into parts once at most kPublishWaves waves of rows are
+// left to hand out (0: once every row has been handed out).
+constexpr unsigned kPublishWaves = SV_PUBLISH_WAVES;
+// A CTA with no rows left looks for draw parts until every request has
+// committed, sleeping kLingerNs between looks, at most kLingerPolls times.
+// Giving up early is harmless: a draw's owner takes its remaining parts.
+constexpr unsigned kLingerNs = 500;
+constexpr unsigned kLingerPolls = 1u << 16;
 
 enum DrawKind { kResidual = 0, kOneHot = 1, kBonus = 2 };
 
@@ -78,14 +140,22 @@ struct Params {
   int32_t* out_len;
   float* out_probs;
   WsHeader* ws;
-  unsigned int* req_done;
-  RowRec* rows;
+  unsigned int* req_done;   // [B] rows finished per request
+  unsigned int* slot_state; // [n_slots] nparts << 20 | parts handed out (0: unpublished)
+  DrawDesc* descs;          // [n_slots]
+  double* tsum;             // [n_slots, tsum_stride] per-tile sums of r
+  int n_slots, tsum_stride;
+  RowRec* rows;             // [R_t]
   long long row_cap;
   int greedy_all;
 };
 
 struct Smem {
-  int item, b, t0, d0, K, i, greedy, xhat, last, stop, pick, pick2, tok;
+  unsigned long long full[kStages];   // stage holds its chunk (bulk-copy bytes landed)
+  unsigned long long empty[kStages];  // every warp has finished reading the stage
+  unsigned ring_seq;                  // chunks this CTA has streamed so far
+  int wk, item, slot, part;
+  int b, t0, d0, K, i, greedy, xhat, last, stop, pick, pick2, tok;
   float redf[kWarps];
   float redf2[kWarps];
   int redi[kWarps];
@@ -112,10 +182,8 @@ struct SoftAcc {
 #pragma unroll
     for (int j = 0; j < EPV; ++j) a[j] = 0.f;
   }
-  __device__ __forceinline__ void add(const float (&f)[EPV], float c) {
-    float vm = f[0];
-#pragma unroll
-    for (int j = 1; j < EPV; ++j) vm = fmaxf(vm, f[j]);
+  // Raises the running maximum to vm (if larger), rescaling the partial sums.
+  __device__ __forceinline__ void raise(float vm, float c) {
     if (vm > m) {
       float nmc = __fmul_rn(vm, c);
       float s = (m == -INFINITY) ? 0.f : ex2(mc - nmc);
@@ -124,81 +192,136 @@ struct SoftAcc {
       m = vm;
       mc = nmc;
     }
+  }
+  __device__ __forceinline__ void add(const float (&f)[EPV], float c) {
+    float vm = f[0];
+#pragma unroll
+    for (int j = 1; j < EPV; ++j) vm = fmaxf(vm, f[j]);
+    raise(vm, c);
 #pragma unroll
     for (int j = 0; j < EPV; ++j) a[j] += ex2(fmaf(f[j], c, -mc));
   }
+  // N vectors at once: one maximum (a shallow tree) and one rescale check.
+  template <int N>
+  __device__ __forceinline__ void add_n(const float (&f)[N][EPV], float c) {
+    float t[N * EPV];
+#pragma unroll
+    for (int u = 0; u < N; ++u)
+#pragma unroll
+      for (int j = 0; j < EPV; ++j) t[u * EPV + j] = f[u][j];
+#pragma unroll
+    for (int w = (N * EPV) / 2; w >= 1; w /= 2)
+#pragma unroll
+      for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+    raise(t[0], c);
+#pragma unroll
+    for (int u = 0; u < N; ++u)
+#pragma unroll
+      for (int j = 0; j < EPV; ++j) a[j] += ex2(fmaf(f[u][j], c, -mc));
+  }
 };
 
-// Streams one row (and optionally its draft row) through the online softmax.
-template <int DT, bool VEC, bool HAS_D>
-__device__ __forceinline__ void stats_pass(const void* trow, const void* drow, int V, float c,
-                                           SoftAcc<Elem<DT>::kEPV>& at,
-                                           SoftAcc<Elem<DT>::kEPV>& ad) {
-  constexpr int EPV = Elem<DT>::kEPV;
-  constexpr int TILE = kThreads * EPV;
-  constexpr int U = HAS_D ? 4 : 8;
-  int x = threadIdx.x * EPV;
-  if constexpr (VEC) {
-    const char* tb = static_cast<const char*>(trow);
-    const char* db = static_cast<const char*>(drow);
-    for (; x + (U - 1) * TILE < V; x += U * TILE) {
-      uint4 rt[U], rd[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        rt[u] = ld_stream16(tb + (size_t)(x + u * TILE) * Elem<DT>::kBytes);
-        if constexpr (HAS_D) rd[u] = ld_stream16(db + (size_t)(x + u * TILE) * Elem<DT>::kBytes);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float f[EPV];
-        Elem<DT>::unpack(rt[u], f);
-        at.add(f, c);
-        if constexpr (HAS_D) {
-          Elem<DT>::unpack(rd[u], f);
-          ad.add(f, c);
-        }
+// ---------------------------------------------------------------------------
+// Bulk-copy ring
+// ---------------------------------------------------------------------------
+// Streams `nbytes` of a row (and the same span of its paired row) through the
+// ring: chunk k lands in stage (seq + k) % kStages and completes on that
+// stage's full barrier; consume(k, stage_addr) is called by every thread once
+// the chunk has arrived, after which each warp releases the stage on its
+// empty barrier. Thread 0 refills a stage only once all warps have released
+// its previous chunk, so warps never wait for each other inside the stream.
+// Every wait is bounded: a warp that gives up leaves the loop (warp-uniformly)
+// and the CTA then agrees on the failure; the copies still in flight are
+// waited for (bounded) and the ring must not be used again. Returns false on
+// such a failure.
+template <class Consume>
+__device__ __forceinline__ bool ring_stream(Smem& s, unsigned char* ring, const char* tptr,
+                                            const char* dptr, size_t nbytes, Consume&& consume) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int nch = (int)((nbytes + kChunkBytes - 1) / kChunkBytes);
+  const unsigned seq0 = s.ring_seq;
+  const uint32_t ring_base = smem_addr(ring);
+  const uint32_t full_base = smem_addr(&s.full[0]);
+  const uint32_t empty_base = smem_addr(&s.empty[0]);
+  int issued = 0;    // chunks issued (thread 0)
+  bool ok = true;    // thread 0's refill waits
+  auto issue = [&](int k) {
+    const unsigned q = seq0 + (unsigned)k;
+    const int st = (int)(q % kStages);
+    // The stage's previous chunk (q - kStages) must have been released.
+    if (q >= (unsigned)kStages && !mbar_wait(empty_base + 8u * st, ((q / kStages) - 1u) & 1u)) {
+      ok = false;
+      return;
+    }
+    const uint32_t bar = full_base + 8u * st;
+    const size_t off = (size_t)k * kChunkBytes;
+    const size_t left = nbytes - off;
+    const uint32_t bytes = (uint32_t)(left < (size_t)kChunkBytes ? left : (size_t)kChunkBytes);
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, dptr ? 2u * bytes : bytes);
+    bulk_g2s(ring_base + (uint32_t)st * kStageBytes, tptr + off, bytes, bar);
+    if (dptr) bulk_g2s(ring_base + (uint32_t)st * kStageBytes + kChunkBytes, dptr + off, bytes, bar);
+    issued = k + 1;
+  };
+  if (tid == 0)
+    for (int k = 0; k < kStages - 1 && k < nch && ok; ++k) issue(k);
+  bool failed = false;
+  for (int k = 0; k < nch; ++k) {
+    if (tid == 0 && ok && k + kStages - 1 < nch) issue(k + kStages - 1);
+    const unsigned q = seq0 + (unsigned)k;
+    const int st = (int)(q % kStages);
+    const bool arrived = mbar_wait(full_base + 8u * st, (q / kStages) & 1u) && ok;
+    if (!__all_sync(kFull, arrived)) {
+      failed = true;
+      break;
+    }
+    consume(k, ring_base + (uint32_t)st * kStageBytes);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_base + 8u * st);
+  }
+  if (__syncthreads_or(failed)) {
+    if (tid == 0) {
+      // Wait (bounded) for every copy this stream issued before giving up.
+      for (int j = 0; j < issued; ++j) {
+        const unsigned q = seq0 + (unsigned)j;
+        mbar_wait(full_base + 8u * (q % kStages), (q / kStages) & 1u);
       }
     }
+    return false;
   }
-  for (; x < V; x += TILE) {
+  if (tid == 0) s.ring_seq = seq0 + (unsigned)nch;
+  __syncthreads();
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Row passes
+// ---------------------------------------------------------------------------
+// Scalar-load variants for rows that are not 16-byte aligned.
+template <int DT, bool HAS_D>
+__device__ __forceinline__ void stats_pass_scalar(const void* trow, const void* drow, int V, float c,
+                                                  SoftAcc<Elem<DT>::kEPV>& at,
+                                                  SoftAcc<Elem<DT>::kEPV>& ad) {
+  constexpr int EPV = Elem<DT>::kEPV;
+  constexpr int TILE = kThreads * EPV;
+  for (int x = threadIdx.x * EPV; x < V; x += TILE) {
     float f[EPV];
-    load_chunk<DT, VEC>(trow, x, V, f);
+    load_chunk<DT, false>(trow, x, V, f);
     at.add(f, c);
     if constexpr (HAS_D) {
-      load_chunk<DT, VEC>(drow, x, V, f);
+      load_chunk<DT, false>(drow, x, V, f);
       ad.add(f, c);
     }
   }
 }
 
-template <int DT, bool VEC>
-__device__ __forceinline__ void argmax_pass(const void* trow, int V, float& bv, int& bi) {
+template <int DT>
+__device__ __forceinline__ void argmax_scalar(const void* trow, int V, float& bv, int& bi) {
   constexpr int EPV = Elem<DT>::kEPV;
   constexpr int TILE = kThreads * EPV;
-  constexpr int U = 8;
-  int x = threadIdx.x * EPV;
-  if constexpr (VEC) {
-    const char* tb = static_cast<const char*>(trow);
-    for (; x + (U - 1) * TILE < V; x += U * TILE) {
-      uint4 rt[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) rt[u] = ld_stream16(tb + (size_t)(x + u * TILE) * Elem<DT>::kBytes);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float f[EPV];
-        Elem<DT>::unpack(rt[u], f);
-#pragma unroll
-        for (int j = 0; j < EPV; ++j)
-          if (f[j] > bv) {
-            bv = f[j];
-            bi = x + u * TILE + j;
-          }
-      }
-    }
-  }
-  for (; x < V; x += TILE) {
+  for (int x = threadIdx.x * EPV; x < V; x += TILE) {
     float f[EPV];
-    load_chunk<DT, VEC>(trow, x, V, f);
+    load_chunk<DT, false>(trow, x, V, f);
 #pragma unroll
     for (int j = 0; j < EPV; ++j)
       if (f[j] > bv) {
@@ -277,94 +400,127 @@ __device__ __forceinline__ int find_request(const int32_t* cu, int B, int t) {
   return lo;
 }
 
-// Inverse-CDF draw at a stop row. Returns the token, or -1 if r has no mass.
+// ---------------------------------------------------------------------------
+// The draw at a stop row
+// ---------------------------------------------------------------------------
+// Everything the draw needs about its stop row.
+struct DrawArgs {
+  const char* trow;
+  const char* drow;  // kResidual only
+  int row, kind, xhat;
+  float mcp, mcq;
+  float bhi, blo;    // beta = S_p / S_q as a double-float pair
+  double u2;
+};
+
+__device__ __forceinline__ DrawArgs make_draw_args(const Params& P, size_t rowb, int row, int drow,
+                                                   int kind, int xhat, float mcp, float mcq,
+                                                   double Sp, double Sq) {
+  DrawArgs a;
+  a.row = row;
+  a.trow = static_cast<const char*>(P.target) + (size_t)row * rowb;
+  a.drow = kind == kResidual ? static_cast<const char*>(P.draft) + (size_t)drow * rowb : nullptr;
+  a.kind = kind;
+  a.xhat = xhat;
+  a.mcp = mcp;
+  a.mcq = mcq;
+  const double beta = kind == kResidual ? Sp / Sq : 1.0;
+  a.bhi = (float)beta;
+  a.blo = (float)(beta - (double)a.bhi);
+  a.u2 = (double)__ldg(&P.uniforms[2 * (size_t)row + 1]);
+  return a;
+}
+
+// r for the EPV elements starting at x. kResidual: max(0, e_p - beta e_q)
+// with beta = S_p / S_q, i.e. S_p * max(0, p - q); otherwise e_p = S_p * p
+// (the rejected one-hot proposal removed).
+template <int EPV>
+__device__ __forceinline__ void residual_of(const DrawArgs& a, float c, const float (&zp)[EPV],
+                                            const float (&zq)[EPV], int x, float (&r)[EPV]) {
+#pragma unroll
+  for (int j = 0; j < EPV; ++j) {
+    const float ep = ex2(fmaf(zp[j], c, -a.mcp));
+    if (a.kind == kResidual) {
+      const float eq = ex2(fmaf(zq[j], c, -a.mcq));
+      float d = fmaf(-eq, a.bhi, ep);
+      d = fmaf(-eq, a.blo, d);
+      r[j] = fmaxf(d, 0.f);
+    } else {
+      r[j] = (a.kind == kOneHot && x + j == a.xhat) ? 0.f : ep;
+    }
+  }
+}
+
+// Sums of r over the warp-sized pieces of tiles [tile0, tile0 + ntl): the
+// total of tile tile0 + l by warp w goes to s.wtot[l * kWarps + w]. Ends with
+// a CTA barrier. Returns false if a bulk copy timed out.
 template <int DT, bool VEC>
-__device__ int draw_token(const Params& P, Smem& s, int kind, const void* trow, const void* drow,
-                          int xhat, float mcp, float mcq, double beta, double u2) {
+__device__ bool tile_sums(const Params& P, Smem& s, unsigned char* ring, const DrawArgs& a,
+                          int tile0, int ntl) {
   constexpr int EPV = Elem<DT>::kEPV;
   constexpr int TILE = kThreads * EPV;
   const int V = P.V;
-  const float c = P.c;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ntiles = (V + TILE - 1) / TILE;
-  const float bhi = (float)beta;
-  const float blo = (float)(beta - (double)bhi);
-
-  // r for the EPV elements starting at x. kResidual: max(0, e_p - beta e_q)
-  // with beta = S_p / S_q, i.e. S_p * max(0, p - q); otherwise e_p = S_p * p.
-  auto r_of = [&](const float (&zp)[EPV], const float (&zq)[EPV], int x, float (&r)[EPV]) {
-#pragma unroll
-    for (int j = 0; j < EPV; ++j) {
-      float ep = ex2(fmaf(zp[j], c, -mcp));
-      if (kind == kResidual) {
-        float eq = ex2(fmaf(zq[j], c, -mcq));
-        float d = fmaf(-eq, bhi, ep);
-        d = fmaf(-eq, blo, d);
-        r[j] = fmaxf(d, 0.f);
-      } else {
-        r[j] = (kind == kOneHot && x + j == xhat) ? 0.f : ep;
-      }
-    }
-  };
-
-  // Pass A: per (tile, warp) sums of r, the warp sum being the last value of
-  // the same Kogge-Stone scan that pass B repeats. The vector path keeps
-  // kScanUnroll tiles of raw 16-byte loads in flight.
-  auto tile_sum = [&](int k, const float (&zp)[EPV], const float (&zq)[EPV]) {
-    const int x = k * TILE + tid * EPV;
+  auto one_tile = [&](int l, const float (&zp)[EPV], const float (&zq)[EPV]) {
+    const int x = (tile0 + l) * TILE + tid * EPV;
     float r[EPV];
-    r_of(zp, zq, x, r);
+    residual_of<EPV>(a, P.c, zp, zq, x, r);
     float ts = 0.f;
 #pragma unroll
     for (int j = 0; j < EPV; ++j) ts += r[j];
     const float inc = warp_incl_scan(ts, lane);
-    if (lane == 31) s.wtot[k * kWarps + warp] = inc;
+    if (lane == 31) s.wtot[l * kWarps + warp] = inc;
   };
   if constexpr (VEC) {
-    const char* tb = static_cast<const char*>(trow);
-    const char* db = static_cast<const char*>(drow);
-    for (int k0 = 0; k0 < ntiles; k0 += kScanUnroll) {
-      uint4 vt[kScanUnroll], vd[kScanUnroll];
+    // Tiles of a chunk are kVPT consecutive tiles; tile0 is chunk aligned.
+    const size_t off = (size_t)tile0 * TILE * Elem<DT>::kBytes;
+    const size_t row_bytes = (size_t)V * Elem<DT>::kBytes;
+    size_t len = (size_t)ntl * TILE * Elem<DT>::kBytes;
+    if (off + len > row_bytes) len = row_bytes - off;
+    const bool res = a.kind == kResidual;
+    return ring_stream(s, ring, a.trow + off, res ? a.drow + off : nullptr, len,
+                       [&](int k, uint32_t stage) {
 #pragma unroll
-      for (int u = 0; u < kScanUnroll; ++u) {
-        const int x = (k0 + u) * TILE + tid * EPV;
-        if (x < V) {
-          vt[u] = ld_stream16(tb + (size_t)x * Elem<DT>::kBytes);
-          if (kind == kResidual) vd[u] = ld_stream16(db + (size_t)x * Elem<DT>::kBytes);
-        }
-      }
+                         for (int v = 0; v < kVPT; ++v) {
+                           const int l = k * kVPT + v;
+                           const int vi = v * kThreads + tid;
+                           const int x = (tile0 + l) * TILE + tid * EPV;
+                           float zp[EPV], zq[EPV];
+                           if (x < V) {
+                             Elem<DT>::unpack(lds16(stage + 16u * vi), zp);
+                             if (res) Elem<DT>::unpack(lds16(stage + kChunkBytes + 16u * vi), zq);
+                           } else {
 #pragma unroll
-      for (int u = 0; u < kScanUnroll; ++u) {
-        if (k0 + u < ntiles) {
-          const int x = (k0 + u) * TILE + tid * EPV;
-          float zp[EPV], zq[EPV];
-          if (x < V) {
-            Elem<DT>::unpack(vt[u], zp);
-            if (kind == kResidual) Elem<DT>::unpack(vd[u], zq);
-          } else {
-#pragma unroll
-            for (int j = 0; j < EPV; ++j) zp[j] = zq[j] = -INFINITY;
-          }
-          tile_sum(k0 + u, zp, zq);
-        }
-      }
-    }
+                             for (int j = 0; j < EPV; ++j) zp[j] = zq[j] = -INFINITY;
+                           }
+                           if (l < ntl) one_tile(l, zp, zq);
+                         }
+                       });
   } else {
-    for (int k = 0; k < ntiles; ++k) {
-      const int x = k * TILE + tid * EPV;
+    for (int l = 0; l < ntl; ++l) {
+      const int x = (tile0 + l) * TILE + tid * EPV;
       float zp[EPV], zq[EPV];
-      load_chunk<DT, VEC>(trow, x, V, zp);
-      if (kind == kResidual) load_chunk<DT, VEC>(drow, x, V, zq);
-      tile_sum(k, zp, zq);
+      load_chunk<DT, false>(a.trow, x, V, zp);
+      if (a.kind == kResidual) load_chunk<DT, false>(a.drow, x, V, zq);
+      one_tile(l, zp, zq);
     }
+    __syncthreads();
+    return true;
   }
-  __syncthreads();
+}
 
-  // Tile sums (warps in order, fp64) and their inclusive prefix over tiles.
-  double tt = 0.0;
-  if (tid < ntiles) {
-    for (int w = 0; w < kWarps; ++w) tt += (double)s.wtot[tid * kWarps + w];
-  }
+// Given this thread's tile sum tt (tile tid < ntiles), finds the tile holding
+// u' * Z and rescans it. Returns the token, or -1 if r has no mass.
+// Tile k spans [tincl[k-1], tincl[k]) of the inclusive prefix of tile sums,
+// so adjacent tiles share their edge; the chosen token is the last index with
+// mass whose lower edge is <= u' * Z, which is the smallest k whose running
+// sum exceeds u' * Z.
+template <int DT, bool VEC>
+__device__ int locate_token(const Params& P, Smem& s, const DrawArgs& a, double tt, int ntiles) {
+  constexpr int EPV = Elem<DT>::kEPV;
+  constexpr int TILE = kThreads * EPV;
+  const int V = P.V;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   double inc = warp_incl_scan_d(tt, lane);
   if (lane == 31) s.dred[warp] = inc;
   __syncthreads();
@@ -379,13 +535,10 @@ __device__ int draw_token(const Params& P, Smem& s, int kind, const void* trow, 
   __syncthreads();
   const double Z = s.tincl[ntiles - 1];
   if (!(Z > 0.0)) return -1;
-  double T = u2 * Z;
+  double T = a.u2 * Z;
   if (!(T >= 0.0)) T = 0.0;  // a NaN or negative uniform draws the first token with mass
-
-  // Tile holding T: the last tile with mass whose lower edge is <= T. Tile k
-  // spans [tincl[k-1], tincl[k]), so adjacent tiles share their edge.
   if (tid < ntiles) {
-    double lo = tid ? s.tincl[tid - 1] : 0.0;
+    const double lo = tid ? s.tincl[tid - 1] : 0.0;
     if (tt > 0.0 && lo <= T) atomicMax(&s.pick, tid);
   }
   __syncthreads();
@@ -393,52 +546,183 @@ __device__ int draw_token(const Params& P, Smem& s, int kind, const void* trow, 
   if (kt < 0) return -1;  // unreachable: the first tile with mass has lower edge 0 <= T
   const double Tk = T - (kt ? s.tincl[kt - 1] : 0.0);
 
-  // Pass B over that tile: thread k spans [wexcl[w] + lane_lo, wexcl[w] + inc).
-  {
-    const int x = kt * TILE + tid * EPV;
-    float zp[EPV], zq[EPV], r[EPV];
-    load_chunk<DT, VEC>(trow, x, V, zp);
-    if (kind == kResidual) load_chunk<DT, VEC>(drow, x, V, zq);
-    r_of(zp, zq, x, r);
-    float ts = 0.f;
+  // The chosen tile: thread k spans [wexcl[w] + lane_lo, wexcl[w] + incl).
+  const int x = kt * TILE + tid * EPV;
+  float zp[EPV], zq[EPV], r[EPV];
+  load_chunk<DT, VEC>(a.trow, x, V, zp);
+  if (a.kind == kResidual) load_chunk<DT, VEC>(a.drow, x, V, zq);
+  residual_of<EPV>(a, P.c, zp, zq, x, r);
+  float ts = 0.f;
 #pragma unroll
-    for (int j = 0; j < EPV; ++j) ts += r[j];
-    float incl = warp_incl_scan(ts, lane);
-    float lane_lo = __shfl_up_sync(kFull, incl, 1);
-    if (lane == 0) lane_lo = 0.f;
-    if (tid == 0) {
-      double acc = 0.0;
-      s.wexcl[0] = 0.0;
-      for (int w = 0; w < kWarps; ++w) {
-        acc = acc + (double)s.wtot[kt * kWarps + w];
-        s.wexcl[w + 1] = acc;
-      }
-      s.pick2 = -1;
-      s.tok = -1;
+  for (int j = 0; j < EPV; ++j) ts += r[j];
+  const float incl = warp_incl_scan(ts, lane);
+  float lane_lo = __shfl_up_sync(kFull, incl, 1);
+  if (lane == 0) lane_lo = 0.f;
+  if (lane == 31) s.redf[warp] = incl;
+  __syncthreads();
+  if (tid == 0) {
+    double acc = 0.0;
+    s.wexcl[0] = 0.0;
+    for (int w = 0; w < kWarps; ++w) {
+      acc = acc + (double)s.redf[w];
+      s.wexcl[w + 1] = acc;
     }
-    __syncthreads();
-    const double lo = s.wexcl[warp] + (double)lane_lo;
-    if (ts > 0.f && lo <= Tk) atomicMax(&s.pick2, tid);
-    __syncthreads();
-    if (tid == s.pick2) {
-      double run = lo;
-      int cand = x;
-#pragma unroll
-      for (int j = 0; j < EPV; ++j) {
-        if (r[j] > 0.f && run <= Tk) cand = x + j;
-        run += (double)r[j];
-      }
-      s.tok = cand;
-    }
-    __syncthreads();
+    s.pick2 = -1;
+    s.tok = -1;
   }
+  __syncthreads();
+  const double lo = s.wexcl[warp] + (double)lane_lo;
+  if (ts > 0.f && lo <= Tk) atomicMax(&s.pick2, tid);
+  __syncthreads();
+  if (tid == s.pick2) {
+    double run = lo;
+    int cand = x;
+#pragma unroll
+    for (int j = 0; j < EPV; ++j) {
+      if (r[j] > 0.f && run <= Tk) cand = x + j;
+      run += (double)r[j];
+    }
+    s.tok = cand;
+  }
+  __syncthreads();
   return s.tok;
 }
 
+// Whole draw by one CTA. Returns the token, -1 if r has no mass, -2 on a
+// copy timeout.
 template <int DT, bool VEC>
-__device__ __noinline__ void commit_request(const Params& P, Smem& s, int b, int t0, int d0, int K, bool greedy) {
+__device__ int draw_whole(const Params& P, Smem& s, unsigned char* ring, const DrawArgs& a) {
+  constexpr int TILE = kThreads * Elem<DT>::kEPV;
+  const int ntiles = (P.V + TILE - 1) / TILE;
+  if (!tile_sums<DT, VEC>(P, s, ring, a, 0, ntiles)) return -2;
+  double tt = 0.0;
+  if (threadIdx.x < ntiles)
+    for (int w = 0; w < kWarps; ++w) tt += (double)s.wtot[threadIdx.x * kWarps + w];
+  return locate_token<DT, VEC>(P, s, a, tt, ntiles);
+}
+
+// Writes the drawn token and (p(y), q(y)) (thread 0).
+template <int DT>
+__device__ void finish_draw(const Params& P, const DrawArgs& a, double Sp, double Sq, int y,
+                            int bonus_row) {
+  float qy;
+  const float zp = Elem<DT>::scalar(a.trow, y);
+  const float py = (float)((double)exp2f(fmaf(zp, P.c, -a.mcp)) / Sp);
+  if (a.kind == kResidual) {
+    const float zq = Elem<DT>::scalar(a.drow, y);
+    qy = (float)((double)exp2f(fmaf(zq, P.c, -a.mcq)) / Sq);
+  } else if (a.kind == kOneHot) {
+    qy = (y == a.xhat) ? 1.f : 0.f;
+  } else {
+    qy = 0.f;
+  }
+  P.out_tokens[a.row] = y;
+  if (P.out_probs) {
+    P.out_probs[2 * (size_t)bonus_row] = py;
+    P.out_probs[2 * (size_t)bonus_row + 1] = qy;
+  }
+}
+
+// Hands out one part of a published draw (thread 0); nothing here waits.
+// Slots are scanned from the head, which moves past every leading slot whose
+// parts are all handed out.
+__device__ bool claim_draw_part(const Params& P, int& slot_out, int& part_out) {
+  unsigned n = ld_relaxed_gpu(&P.ws->n_draws);
+  if (n > (unsigned)P.n_slots) n = (unsigned)P.n_slots;
+  const unsigned h = ld_relaxed_gpu(&P.ws->draw_head);
+  unsigned adv = h;
+  bool leading = true;
+  for (unsigned i = h; i < n; ++i) {
+    const unsigned v = ld_acquire_gpu(&P.slot_state[i]);
+    const unsigned np = v >> kSlotCountBits;
+    if (np == 0u) {  // reserved, not yet published
+      leading = false;
+      continue;
+    }
+    if ((v & kSlotCountMask) < np) {
+      const unsigned pt = atomicAdd(&P.slot_state[i], 1u) & kSlotCountMask;
+      if (pt < np) {
+        if (leading && pt + 1u == np) adv = i + 1;
+        if (adv > h) atomicMax(&P.ws->draw_head, adv);
+        slot_out = (int)i;
+        part_out = (int)pt;
+        return true;
+      }
+    }
+    if (leading) adv = i + 1;
+  }
+  if (adv > h) atomicMax(&P.ws->draw_head, adv);
+  return false;
+}
+
+// One part of the draw in `slot`: sums of r over the part's tiles go to the
+// workspace; the CTA that finishes the draw's last part locates the token.
+// Returns false if a bulk copy timed out.
+template <int DT, bool VEC>
+__device__ __noinline__ bool draw_part(const Params& P, Smem& s, unsigned char* ring, int slot,
+                                       int part) {
+  constexpr int TILE = kThreads * Elem<DT>::kEPV;
   const int tid = threadIdx.x;
-  const size_t rowb = (size_t)P.V * Elem<DT>::kBytes;
+  const DrawDesc* d = &P.descs[slot];
+  const double Sp = __ldcg(&d->Sp), Sq = __ldcg(&d->Sq);
+  const int kind = __ldcg(&d->kind);
+  const DrawArgs a = make_draw_args(P, (size_t)P.V * Elem<DT>::kBytes, __ldcg(&d->row),
+                                    __ldcg(&d->drow), kind, __ldcg(&d->xhat), __ldcg(&d->mcp),
+                                    __ldcg(&d->mcq), Sp, Sq);
+  const int nparts = __ldcg(&d->nparts);
+  const int ntiles = (P.V + TILE - 1) / TILE;
+  // Parts are whole ring chunks (kVPT tiles each).
+  const int nchunks = (ntiles + kVPT - 1) / kVPT;
+  const int cpp = (nchunks + nparts - 1) / nparts;
+  const int tile0 = part * cpp * kVPT;
+  const int tile1 = min(ntiles, (part + 1) * cpp * kVPT);
+  const int ntl = tile1 - tile0;
+  double* tsum = P.tsum + (size_t)slot * P.tsum_stride;
+  if (ntl > 0) {
+    if (!tile_sums<DT, VEC>(P, s, ring, a, tile0, ntl)) return false;
+    if (tid < ntl) {
+      double tt = 0.0;
+      for (int w = 0; w < kWarps; ++w) tt += (double)s.wtot[tid * kWarps + w];
+      tsum[tile0 + tid] = tt;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned old = atomicAdd(&P.descs[slot].done, 1u);
+    s.last = (old == (unsigned)nparts - 1u) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s.last) return true;
+  // Last part: every tile sum is in the workspace.
+  __threadfence();
+  const double tt = tid < ntiles ? __ldcg(&tsum[tid]) : 0.0;
+  int y = locate_token<DT, VEC>(P, s, a, tt, ntiles);
+  DrawArgs used = a;
+  if (y < 0 && kind != kBonus) {
+    // No residual mass (p == q in fp32): draw from p instead.
+    if (tid == 0) atomicOr(&P.ws->status, SV_DATA_DEGENERATE_RESIDUAL);
+    used.kind = kBonus;
+    used.bhi = 1.f;
+    used.blo = 0.f;
+    y = draw_whole<DT, VEC>(P, s, ring, used);
+    if (y == -2) return false;
+  }
+  if (y < 0) {
+    if (tid == 0) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
+    y = 0;
+  }
+  if (tid == 0) finish_draw<DT>(P, used, Sp, Sq, y, __ldcg(&d->bonus_row));
+  return true;
+}
+
+// Commit of request b by the CTA that finished its last row: stop slot,
+// accepted drafts, length and the final token (the argmax for a greedy
+// request, the draw for a sampled one). Returns false if a bulk copy timed out.
+template <int DT, bool VEC>
+__device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned char* ring, int b,
+                                            int t0, int d0, int K, bool greedy) {
+  const int tid = threadIdx.x;
   if (tid == 0) {
     __threadfence();
     int stop = K;
@@ -454,68 +738,104 @@ __device__ __noinline__ void commit_request(const Params& P, Smem& s, int b, int
   const int stop = s.stop;
   for (int j = tid; j < stop; j += kThreads) P.out_tokens[t0 + j] = P.draft_tokens[d0 + j];
   const int srow = t0 + stop;
-  int y;
-  float py = -1.f, qy = -1.f;
-  if (greedy) {
-    y = __ldcg(&P.rows[srow].argmax);
-  } else {
-    const float mcp = __ldcg(&P.rows[srow].mc_p);
-    const float mcq = __ldcg(&P.rows[srow].mc_q);
-    const double Sp = __ldcg(&P.rows[srow].S_p);
-    const double Sq = __ldcg(&P.rows[srow].S_q);
-    const char* trow = static_cast<const char*>(P.target) + (size_t)srow * rowb;
-    const char* drow = nullptr;
-    int kind = kBonus, xhat = -1;
-    if (stop < K) {
-      xhat = P.draft_tokens[d0 + stop];
-      if (xhat < 0 || xhat >= P.V) xhat = -1;
-      if (P.draft) {
-        kind = kResidual;
-        drow = static_cast<const char*>(P.draft) + (size_t)(d0 + stop) * rowb;
-      } else {
-        kind = kOneHot;
-      }
-    }
-    const double u2 = (double)__ldg(&P.uniforms[2 * (size_t)srow + 1]);
-    y = draw_token<DT, VEC>(P, s, kind, trow, drow, xhat, mcp, mcq,
-                            kind == kResidual ? Sp / Sq : 1.0, u2);
-    if (y < 0 && kind != kBonus) {
-      // No residual mass (p == q in fp32): draw from p instead.
-      if (tid == 0) atomicOr(&P.ws->status, SV_DATA_DEGENERATE_RESIDUAL);
-      kind = kBonus;
-      y = draw_token<DT, VEC>(P, s, kind, trow, drow, xhat, mcp, mcq, 1.0, u2);
-    }
-    if (y < 0) {
-      if (tid == 0) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
-      y = 0;
-    }
-    if (tid == 0) {
-      float zp = Elem<DT>::scalar(trow, y);
-      py = (float)((double)exp2f(fmaf(zp, P.c, -mcp)) / Sp);
-      if (kind == kResidual) {
-        float zq = Elem<DT>::scalar(drow, y);
-        qy = (float)((double)exp2f(fmaf(zq, P.c, -mcq)) / Sq);
-      } else if (kind == kOneHot) {
-        qy = (y == xhat) ? 1.f : 0.f;
-      } else {
-        qy = 0.f;
-      }
-    }
-  }
   if (tid == 0) {
-    P.out_tokens[srow] = y;
     P.out_len[b] = stop + 1;
-    if (P.out_probs) {
-      P.out_probs[2 * (size_t)(t0 + K)] = py;
-      P.out_probs[2 * (size_t)(t0 + K) + 1] = qy;
-    }
     P.req_done[b] = 0u;
+    atomicAdd(&P.ws->committed, 1u);
   }
+  if (greedy) {
+    if (tid == 0) {
+      P.out_tokens[srow] = __ldcg(&P.rows[srow].argmax);
+      if (P.out_probs) {
+        P.out_probs[2 * (size_t)(t0 + K)] = -1.f;
+        P.out_probs[2 * (size_t)(t0 + K) + 1] = -1.f;
+      }
+    }
+    return true;
+  }
+  int kind = kBonus, xhat = -1, drow = -1;
+  if (stop < K) {
+    xhat = P.draft_tokens[d0 + stop];
+    if (xhat < 0 || xhat >= P.V) xhat = -1;
+    if (P.draft) {
+      kind = kResidual;
+      drow = d0 + stop;
+    } else {
+      kind = kOneHot;
+    }
+  }
+  const double Sp = __ldcg(&P.rows[srow].S_p), Sq = __ldcg(&P.rows[srow].S_q);
+  const float mcp = __ldcg(&P.rows[srow].mc_p), mcq = __ldcg(&P.rows[srow].mc_q);
+  // Once the rows left fit in one wave, CTAs are about to fall idle: publish
+  // the draw in parts so that they can share it, and take parts of it here.
+  if (tid == 0) {
+    constexpr int TILE = kThreads * Elem<DT>::kEPV;
+    const int nchunks = ((P.V + TILE - 1) / TILE + kVPT - 1) / kVPT;
+    int nparts = (nchunks + kPartChunks - 1) / kPartChunks;
+    nparts = nparts > kMaxParts ? kMaxParts : nparts;
+    s.slot = -1;
+    if (nparts > 1 && ld_relaxed_gpu(&P.ws->next_item) + kPublishWaves * gridDim.x >=
+                          (unsigned)(P.cu[P.B] + P.B)) {
+      const unsigned slot = atomicAdd(&P.ws->n_draws, 1u);
+      if (slot < (unsigned)P.n_slots) {
+        DrawDesc* d = &P.descs[slot];
+        d->b = b;
+        d->row = srow;
+        d->drow = drow;
+        d->kind = kind;
+        d->xhat = xhat;
+        d->mcp = mcp;
+        d->mcq = mcq;
+        d->nparts = nparts;
+        d->Sp = Sp;
+        d->Sq = Sq;
+        d->bonus_row = t0 + K;
+        __threadfence();
+        st_release_gpu(&P.slot_state[slot], (unsigned)nparts << kSlotCountBits);
+        s.slot = (int)slot;
+      }
+    }
+  }
+  __syncthreads();
+  if (s.slot >= 0) {
+    const int slot = s.slot;
+    for (;;) {
+      __syncthreads();
+      if (tid == 0) s.part = (int)(atomicAdd(&P.slot_state[slot], 1u) & kSlotCountMask);
+      __syncthreads();
+      const int part = s.part;
+      if (part >= __ldcg(&P.descs[slot].nparts)) break;
+      if (!draw_part<DT, VEC>(P, s, ring, slot, part)) return false;
+    }
+    return true;
+  }
+  const DrawArgs a = make_draw_args(P, (size_t)P.V * Elem<DT>::kBytes, srow, drow, kind, xhat, mcp,
+                                    mcq, Sp, Sq);
+  int y = draw_whole<DT, VEC>(P, s, ring, a);
+  if (y == -2) return false;
+  DrawArgs used = a;
+  if (y < 0 && kind != kBonus) {
+    // No residual mass (p == q in fp32): draw from p instead.
+    if (tid == 0) atomicOr(&P.ws->status, SV_DATA_DEGENERATE_RESIDUAL);
+    used.kind = kBonus;
+    used.bhi = 1.f;
+    used.blo = 0.f;
+    y = draw_whole<DT, VEC>(P, s, ring, used);
+    if (y == -2) return false;
+  }
+  if (y < 0) {
+    if (tid == 0) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
+    y = 0;
+  }
+  if (tid == 0) finish_draw<DT>(P, used, Sp, Sq, y, t0 + K);
+  return true;
 }
 
+// One row. Returns false if a bulk copy timed out.
 template <int DT, bool VEC>
-__device__ void process_row(const Params& P, Smem& s, int t) {
+__device__ bool process_row(const Params& P, Smem& s, unsigned char* ring, int t) {
   constexpr int EPV = Elem<DT>::kEPV;
+  constexpr int CH = kChunkBytes / Elem<DT>::kBytes;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     const int b = find_request(P.cu, P.B, t);
@@ -549,13 +869,35 @@ __device__ void process_row(const Params& P, Smem& s, int t) {
   __syncthreads();
   const int b = s.b, t0 = s.t0, d0 = s.d0, K = s.K, i = s.i, xhat = s.xhat;
   const bool greedy = s.greedy != 0;
-  const size_t rowb = (size_t)P.V * Elem<DT>::kBytes;
+  const int V = P.V;
+  const size_t rowb = (size_t)V * Elem<DT>::kBytes;
   const char* trow = static_cast<const char*>(P.target) + (size_t)t * rowb;
+  bool ok = true;
   RowRec rec;
   if (greedy) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    argmax_pass<DT, VEC>(trow, P.V, bv, bi);
+    if constexpr (VEC) {
+      ok = ring_stream(s, ring, trow, nullptr, rowb, [&](int k, uint32_t stage) {
+#pragma unroll
+        for (int v = 0; v < kVPT; ++v) {
+          const int vi = v * kThreads + tid;
+          const int x = k * CH + vi * EPV;
+          if (x < V) {
+            float f[EPV];
+            Elem<DT>::unpack(lds16(stage + 16u * vi), f);
+#pragma unroll
+            for (int j = 0; j < EPV; ++j)
+              if (f[j] > bv) {
+                bv = f[j];
+                bi = x + j;
+              }
+          }
+        }
+      });
+    } else {
+      argmax_scalar<DT>(trow, V, bv, bi);
+    }
     warp_argmax(bv, bi);
     if (lane == 0) {
       s.redf[warp] = bv;
@@ -584,10 +926,40 @@ __device__ void process_row(const Params& P, Smem& s, int t) {
     SoftAcc<EPV> at, ad;
     at.init();
     ad.init();
-    if (has_d)
-      stats_pass<DT, VEC, true>(trow, drow, P.V, P.c, at, ad);
-    else
-      stats_pass<DT, VEC, false>(trow, drow, P.V, P.c, at, ad);
+    if constexpr (VEC) {
+      ok = ring_stream(s, ring, trow, drow, rowb, [&](int k, uint32_t stage) {
+        float f[kVPT][EPV];
+#pragma unroll
+        for (int v = 0; v < kVPT; ++v) {
+          const int vi = v * kThreads + tid;
+          if (k * CH + vi * EPV < V) {
+            Elem<DT>::unpack(lds16(stage + 16u * vi), f[v]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) f[v][j] = -INFINITY;
+          }
+        }
+        at.add_n<kVPT>(f, P.c);
+        if (has_d) {
+#pragma unroll
+          for (int v = 0; v < kVPT; ++v) {
+            const int vi = v * kThreads + tid;
+            if (k * CH + vi * EPV < V) {
+              Elem<DT>::unpack(lds16(stage + kChunkBytes + 16u * vi), f[v]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < EPV; ++j) f[v][j] = -INFINITY;
+            }
+          }
+          ad.add_n<kVPT>(f, P.c);
+        }
+      });
+    } else {
+      if (has_d)
+        stats_pass_scalar<DT, true>(trow, drow, V, P.c, at, ad);
+      else
+        stats_pass_scalar<DT, false>(trow, drow, V, P.c, at, ad);
+    }
     float mcp, mcq;
     double Sp, Sq;
     combine_softmax<EPV>(at, ad, has_d, P.c, s, mcp, Sp, mcq, Sq);
@@ -631,6 +1003,7 @@ __device__ void process_row(const Params& P, Smem& s, int t) {
       }
     }
   }
+  if (!ok) return false;
   if (tid == 0) {
     P.rows[t] = rec;
     __threadfence();
@@ -638,13 +1011,15 @@ __device__ void process_row(const Params& P, Smem& s, int t) {
     s.last = (old == (unsigned)K) ? 1 : 0;
   }
   __syncthreads();
-  if (s.last) commit_request<DT, VEC>(P, s, b, t0, d0, K, greedy);
+  if (s.last) ok = commit_request<DT, VEC>(P, s, ring, b, t0, d0, K, greedy);
   __syncthreads();
+  return ok;
 }
 
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads, 2) verify_kernel(Params P) {
+__global__ void __launch_bounds__(kThreads, SV_MINBLOCKS) verify_kernel(Params P) {
   __shared__ Smem s;
+  extern __shared__ __align__(128) unsigned char ring[];
   const int tid = threadIdx.x;
   // Offsets must be a valid packed layout that fits the workspace; every CTA
   // checks and all of them take the same decision.
@@ -654,26 +1029,79 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(Params P) {
   if (tid == 0) {
     if (P.cu[0] != 0) bad = true;
     if ((long long)P.cu[P.B] + P.B > P.row_cap) bad = true;
+    if constexpr (VEC) {
+      for (int j = 0; j < kStages; ++j) {
+        mbar_init(smem_addr(&s.full[j]), 1);
+        mbar_init(smem_addr(&s.empty[j]), kWarps);
+      }
+      fence_mbar_init();
+    }
+    s.ring_seq = 0;
   }
   if (__syncthreads_or(bad)) {
     if (blockIdx.x == 0 && tid == 0) atomicOr(&P.ws->status, SV_DATA_BAD_OFFSETS);
     return;
   }
-  const int R_t = P.cu[P.B] + P.B;
+  const unsigned R_t = (unsigned)(P.cu[P.B] + P.B);
   for (;;) {
-    if (tid == 0) s.item = (int)atomicAdd(&P.ws->next_item, 1u);
+    if (tid == 0) {
+      // Rows first; once they are all handed out, parts of published draws.
+      int slot = -1, part = -1;
+      const unsigned t = atomicAdd(&P.ws->next_item, 1u);
+      s.wk = 0;
+      if (t < R_t) {
+        s.wk = 2;
+        s.item = (int)t;
+      } else {
+        for (unsigned poll = 0; poll < kLingerPolls; ++poll) {
+          if (claim_draw_part(P, slot, part)) {
+            s.wk = 1;
+            break;
+          }
+          if (ld_relaxed_gpu(&P.ws->committed) >= (unsigned)P.B) {
+            if (claim_draw_part(P, slot, part)) s.wk = 1;
+            break;
+          }
+          __nanosleep(kLingerNs);
+        }
+      }
+      s.slot = slot;
+      s.part = part;
+    }
     __syncthreads();
-    const int t = s.item;
+    const int wk = s.wk, item = s.item, slot = s.slot, part = s.part;
     __syncthreads();
-    if (t >= R_t) break;
-    process_row<DT, VEC>(P, s, t);
+    if (wk == 0) break;
+    const bool ok = wk == 2 ? process_row<DT, VEC>(P, s, ring, item)
+                            : draw_part<DT, VEC>(P, s, ring, slot, part);
+    if (!ok) {
+      // A bulk copy never completed: report it and leave without touching
+      // the shared counters (the workspace must be zero-filled again).
+      if (tid == 0) atomicOr(&P.ws->status, SV_DEV_COPY_TIMEOUT);
+      return;
+    }
+  }
+  // The last CTA to leave clears the draw slots and the counters.
+  if (tid == 0) {
+    __threadfence();
+    const unsigned old = atomicAdd(&P.ws->exited, 1u);
+    s.last = (old == gridDim.x - 1) ? 1 : 0;
+    if (s.last) __threadfence();
+  }
+  __syncthreads();
+  if (!s.last) return;
+  unsigned n = __ldcg(&P.ws->n_draws);
+  if (n > (unsigned)P.n_slots) n = (unsigned)P.n_slots;
+  for (unsigned k = tid; k < n; k += kThreads) {
+    P.slot_state[k] = 0u;
+    P.descs[k].done = 0u;
   }
   if (tid == 0) {
-    const unsigned old = atomicAdd(&P.ws->exited, 1u);
-    if (old == gridDim.x - 1) {
-      P.ws->next_item = 0u;
-      P.ws->exited = 0u;
-    }
+    P.ws->next_item = 0u;
+    P.ws->n_draws = 0u;
+    P.ws->draw_head = 0u;
+    P.ws->committed = 0u;
+    P.ws->exited = 0u;
   }
 }
 
@@ -682,13 +1110,38 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(Params P) {
 // ---------------------------------------------------------------------------
 static size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-static size_t ws_size(long long B, long long R_t) {
-  return sizeof(WsHeader) + align16((size_t)B * sizeof(unsigned)) + (size_t)R_t * sizeof(RowRec);
+// Draw slots (parts of draws published near the end of a call), and tile
+// sums per slot counted with the smaller fp32 tile so one size fits both types.
+static int n_draw_slots(long long B) { return (int)(B < kMaxDrawSlots ? B : kMaxDrawSlots); }
+static int tsum_stride(int V) { return (V + kThreads * 4 - 1) / (kThreads * 4); }
+
+// header | req_done[B] | slot_state[S] | descs[S] | tsum[S][stride] | rows[R_t]
+struct WsLayout {
+  size_t req_done, slot_state, descs, tsum, rows;
+};
+
+static WsLayout ws_layout(long long B, int V) {
+  const size_t S = (size_t)n_draw_slots(B);
+  WsLayout L;
+  L.req_done = sizeof(WsHeader);
+  L.slot_state = L.req_done + align16((size_t)B * sizeof(unsigned));
+  L.descs = L.slot_state + align16(S * sizeof(unsigned));
+  L.tsum = L.descs + S * sizeof(DrawDesc);
+  L.rows = L.tsum + align16(S * (size_t)tsum_stride(V) * sizeof(double));
+  return L;
 }
 
-// Resident CTAs per device for each kernel variant, filled on first use.
+static size_t ws_size(long long B, long long R_t, int V) {
+  return ws_layout(B, V).rows + (size_t)R_t * sizeof(RowRec);
+}
+
+// Resident CTAs per device for each kernel variant, filled on first use
+// (which also raises the variant's dynamic shared-memory limit).
 constexpr int kMaxDevices = 64;
 static std::atomic<int> g_resident[kMaxDevices][2][2];
+
+template <bool VEC>
+static constexpr int dyn_smem() { return VEC ? kRingBytes : 0; }
 
 template <int DT, bool VEC>
 static cudaError_t resident_ctas(int dev, int* out) {
@@ -697,10 +1150,14 @@ static cudaError_t resident_ctas(int dev, int* out) {
     *out = cached;
     return cudaSuccess;
   }
-  int sms = 0, per_sm = 0;
-  cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = cudaFuncSetAttribute(verify_kernel<DT, VEC>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<VEC>());
   if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<DT, VEC>, kThreads, 0);
+  int sms = 0, per_sm = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<DT, VEC>, kThreads,
+                                                    dyn_smem<VEC>());
   if (e != cudaSuccess) return e;
   const int n = sms * (per_sm > 0 ? per_sm : 1);
   if (dev < kMaxDevices) g_resident[dev][DT][VEC].store(n, std::memory_order_relaxed);
@@ -718,7 +1175,7 @@ static cudaError_t launch(const Params& P, cudaStream_t st) {
   long long grid = resident;
   if (grid > P.row_cap) grid = P.row_cap;
   if (grid < 1) grid = 1;
-  verify_kernel<DT, VEC><<<(unsigned)grid, kThreads, 0, st>>>(P);
+  verify_kernel<DT, VEC><<<(unsigned)grid, kThreads, dyn_smem<VEC>(), st>>>(P);
   return cudaGetLastError();
 }
 
@@ -742,9 +1199,10 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
       (uintptr_t)out_len % 4 || (out_probs && (uintptr_t)out_probs % 4) ||
       (uniforms && (uintptr_t)uniforms % 4) || (draft_tokens && (uintptr_t)draft_tokens % 4))
     return SV_ERR_INVALID_ARG;
-  const size_t fixed = sizeof(WsHeader) + align16((size_t)B * sizeof(unsigned));
-  if (workspace_bytes < fixed + sizeof(RowRec)) return SV_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(B, V);
+  if (workspace_bytes < L.rows + sizeof(RowRec)) return SV_ERR_INVALID_ARG;
 
+  char* ws = static_cast<char*>(workspace);
   Params P;
   P.target = target;
   P.draft = greedy_all ? nullptr : draft;
@@ -758,12 +1216,18 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
   P.out_tokens = out_tokens;
   P.out_len = out_len;
   P.out_probs = greedy_all ? nullptr : out_probs;
-  P.ws = static_cast<WsHeader*>(workspace);
-  P.req_done = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + sizeof(WsHeader));
-  P.rows = reinterpret_cast<RowRec*>(static_cast<char*>(workspace) + fixed);
-  P.row_cap = (long long)((workspace_bytes - fixed) / sizeof(RowRec));
+  P.ws = reinterpret_cast<WsHeader*>(ws);
+  P.req_done = reinterpret_cast<unsigned*>(ws + L.req_done);
+  P.slot_state = reinterpret_cast<unsigned*>(ws + L.slot_state);
+  P.descs = reinterpret_cast<DrawDesc*>(ws + L.descs);
+  P.tsum = reinterpret_cast<double*>(ws + L.tsum);
+  P.n_slots = n_draw_slots(B);
+  P.tsum_stride = tsum_stride(V);
+  P.rows = reinterpret_cast<RowRec*>(ws + L.rows);
+  P.row_cap = (long long)((workspace_bytes - L.rows) / sizeof(RowRec));
   P.greedy_all = greedy_all;
 
+  // Bulk copies need 16-byte aligned row starts and 16-byte multiples.
   const bool vec = ((uintptr_t)target % 16 == 0) && (!P.draft || (uintptr_t)P.draft % 16 == 0) &&
                    (((size_t)V * es) % 16 == 0);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -779,9 +1243,9 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
 
 extern "C" {
 
-size_t spec_verify_workspace_size(int32_t B, int32_t R_t) {
-  if (B < 0 || R_t < 0) return 0;
-  return sv::ws_size(B, R_t > 0 ? R_t : 1);
+size_t spec_verify_workspace_size(int32_t B, int32_t R_t, int32_t V) {
+  if (B < 0 || R_t < 0 || V < 1) return 0;
+  return sv::ws_size(B, R_t > 0 ? R_t : 1, V);
 }
 
 sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dtype dtype,
@@ -813,6 +1277,7 @@ sv_status sv_check_status(void* workspace, void* cuda_stream, uint32_t* out_bits
   if (cudaStreamSynchronize(st) != cudaSuccess) return SV_ERR_CUDA;
   if (cudaMemsetAsync(workspace, 0, sizeof bits, st) != cudaSuccess) return SV_ERR_CUDA;
   *out_bits = bits;
+  if (bits & SV_DEV_COPY_TIMEOUT) return SV_ERR_TIMEOUT;
   return (bits & ~SV_DATA_DEGENERATE_RESIDUAL) ? SV_ERR_DATA : SV_OK;
 }
 

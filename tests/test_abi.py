@@ -30,9 +30,14 @@ def test_exports_every_declared_function(lib):
 
 
 def test_workspace_size(lib):
-    for B, R in [(1, 5), (64, 384), (256, 2048), (513, 3000)]:
-        assert api.spec_verify_workspace_size(B, R) == 64 + ((4 * B + 15) // 16) * 16 + 32 * R
-    assert lib.spec_verify_workspace_size(-1, 4) == 0
+    a16 = lambda x: (x + 15) // 16 * 16
+    for B, R, V in [(1, 5, 32000), (64, 384, 128256), (256, 2048, 151936), (513, 3000, 256000), (7, 9, 1)]:
+        S = min(B, 4096)            # draw slots
+        tiles = (V + 1023) // 1024  # tile sums per slot (fp32-sized tiles)
+        want = 64 + a16(4 * B) + a16(4 * S) + 64 * S + a16(8 * S * tiles) + 32 * R
+        assert api.spec_verify_workspace_size(B, R, V) == want
+    assert lib.spec_verify_workspace_size(-1, 4, 10) == 0
+    assert lib.spec_verify_workspace_size(4, 4, 0) == 0
 
 
 def test_status_strings(lib):

@@ -24,7 +24,7 @@ def _run(batch, workspace=None):
 # --------------------------------------------------------------------------
 def test_config1_sampling_1000_rounds(cuda_lib):
     """B=1, K=4, V=32000 fp32, T=1: 1000 rounds of fresh logits, one workspace."""
-    ws = api.new_workspace(1, 5)
+    ws = api.new_workspace(1, 5, 32000)
     mism = flagged = rows = 0
     for r in range(1000):
         rep, _, _ = _run(W.config1(seed=101, round_index=r), ws)
@@ -173,7 +173,7 @@ def test_rerun_is_bit_identical(cuda_lib):
 
 def test_data_errors_set_status_and_leave_workspace_usable(cuda_lib):
     b = W.gaussian_sampling(seed=304, B=8, K=3, V=512, sigma=1.0, draft_sigma=0.5, T=1.0)
-    ws = api.new_workspace(b.B, b.R_t)
+    ws = api.new_workspace(b.B, b.R_t, b.V)
     db = parity.to_device(b)
     bad = db.draft_tokens.clone()
     bad[2] = 512  # out of range
