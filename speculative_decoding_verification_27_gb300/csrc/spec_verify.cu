@@ -65,6 +65,16 @@ struct alignas(16) RowRec {
 };
 static_assert(sizeof(RowRec) == 32, "row record is 32 bytes");
 
+// Statistics of one part of a split row (32 bytes): the same quantities as
+// RowRec over the part's slice, S = 0 for a slice without a finite logit.
+struct alignas(16) PartRec {
+  float mc_p, mc_q;
+  double S_p, S_q;
+  float amax_v;      // greedy: largest logit of the slice
+  int amax_i;        // and its first index (0x7fffffff if none)
+};
+static_assert(sizeof(PartRec) == 32, "part record is 32 bytes");
+
 // A draw published in parts (64 bytes); `done` counts finished parts. The
 // slot's state word packs the part count (bits 20..31, 0 = not published)
 // and the parts handed out (bits 0..19), so one load checks a slot and one
@@ -108,6 +118,12 @@ constexpr int max_vocab(int dtype) { return kMaxScanTiles * kThreads * (dtype ==
 #ifndef SV_PUBLISH_WAVES
 #define SV_PUBLISH_WAVES 0
 #endif
+#ifndef SV_ROW_PARTS
+#define SV_ROW_PARTS 1
+#endif
+#ifndef SV_TAIL_WAVES
+#define SV_TAIL_WAVES 1
+#endif
 constexpr int kStages = SV_STAGES;                  // stages (kStages - 1 in flight)
 constexpr int kVPT = SV_VPT;                        // 16-byte vectors per thread per chunk
 constexpr int kChunkBytes = kThreads * 16 * kVPT;   // bytes of one row per stage
@@ -119,6 +135,16 @@ constexpr int kMaxDrawSlots = 4096;                 // draws that can be publish
 // Draws are split into parts once at most kPublishWaves waves of rows are
 // left to hand out (0: once every row has been handed out).
 constexpr unsigned kPublishWaves = SV_PUBLISH_WAVES;
+// Rows may be split into parts that different CTAs stream; the CTA that
+// finishes a row's last part merges the parts' statistics. Every row is
+// split when there are fewer rows than CTAs (small batches); the last
+// kTailWaves waves of a large batch are split when kRowParts > 1 (measured
+// slower on the benchmark workload, so off by default).
+constexpr unsigned kRowParts = SV_ROW_PARTS;        // parts per split row (large batches)
+constexpr unsigned kTailWaves = SV_TAIL_WAVES;
+constexpr unsigned kMaxRowParts = 16;
+constexpr unsigned kMaxTailRows = 4096;             // split rows per call, at most
+constexpr unsigned kMaxPartRecs = 16384;            // part records, at most
 // A CTA with no rows left looks for draw parts until every request has
 // committed, sleeping kLingerNs between looks, at most kLingerPolls times.
 // Giving up early is harmless: a draw's owner takes its remaining parts.
@@ -140,11 +166,13 @@ struct Params {
   int32_t* out_len;
   float* out_probs;
   WsHeader* ws;
-  unsigned int* req_done;   // [B] rows finished per request
+  unsigned long long* req_state;  // [B] rows finished (and accepted) per request
   unsigned int* slot_state; // [n_slots] nparts << 20 | parts handed out (0: unpublished)
   DrawDesc* descs;          // [n_slots]
   double* tsum;             // [n_slots, tsum_stride] per-tile sums of r
   int n_slots, tsum_stride;
+  unsigned int* part_done;  // [kMaxTailRows] parts finished per split row
+  PartRec* parts;           // [kMaxPartRecs]
   RowRec* rows;             // [R_t]
   long long row_cap;
   int greedy_all;
@@ -155,7 +183,8 @@ struct Smem {
   unsigned long long empty[kStages];  // every warp has finished reading the stage
   unsigned ring_seq;                  // chunks this CTA has streamed so far
   int wk, item, slot, part;
-  int b, t0, d0, K, i, greedy, xhat, last, stop, pick, pick2, tok;
+  unsigned n_items, r_full, row_parts;  // work-item layout of this launch
+  int b, t0, d0, K, i, greedy, xhat, last, stop, merge, pick, pick2, tok;
   float redf[kWarps];
   float redf2[kWarps];
   int redi[kWarps];
@@ -225,7 +254,9 @@ struct SoftAcc {
 // Bulk-copy ring
 // ---------------------------------------------------------------------------
 // Streams `nbytes` of a row (and the same span of its paired row) through the
-// ring: chunk k lands in stage (seq + k) % kStages and completes on that
+// ring, first chunk first or (reverse) last chunk first; consume() gets the
+// chunk's index in the span. The k-th chunk streamed lands in stage
+// (seq + k) % kStages and completes on that
 // stage's full barrier; consume(k, stage_addr) is called by every thread once
 // the chunk has arrived, after which each warp releases the stage on its
 // empty barrier. Thread 0 refills a stage only once all warps have released
@@ -236,7 +267,8 @@ struct SoftAcc {
 // such a failure.
 template <class Consume>
 __device__ __forceinline__ bool ring_stream(Smem& s, unsigned char* ring, const char* tptr,
-                                            const char* dptr, size_t nbytes, Consume&& consume) {
+                                            const char* dptr, size_t nbytes, bool reverse,
+                                            Consume&& consume) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int nch = (int)((nbytes + kChunkBytes - 1) / kChunkBytes);
   const unsigned seq0 = s.ring_seq;
@@ -254,7 +286,7 @@ __device__ __forceinline__ bool ring_stream(Smem& s, unsigned char* ring, const 
       return;
     }
     const uint32_t bar = full_base + 8u * st;
-    const size_t off = (size_t)k * kChunkBytes;
+    const size_t off = (size_t)(reverse ? nch - 1 - k : k) * kChunkBytes;
     const size_t left = nbytes - off;
     const uint32_t bytes = (uint32_t)(left < (size_t)kChunkBytes ? left : (size_t)kChunkBytes);
     fence_proxy_async_smem();
@@ -275,7 +307,7 @@ __device__ __forceinline__ bool ring_stream(Smem& s, unsigned char* ring, const 
       failed = true;
       break;
     }
-    consume(k, ring_base + (uint32_t)st * kStageBytes);
+    consume(reverse ? nch - 1 - k : k, ring_base + (uint32_t)st * kStageBytes);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_base + 8u * st);
   }
@@ -478,7 +510,9 @@ __device__ bool tile_sums(const Params& P, Smem& s, unsigned char* ring, const D
     size_t len = (size_t)ntl * TILE * Elem<DT>::kBytes;
     if (off + len > row_bytes) len = row_bytes - off;
     const bool res = a.kind == kResidual;
-    return ring_stream(s, ring, a.trow + off, res ? a.drow + off : nullptr, len,
+    // Last chunk first: the end of the stop row was streamed most recently by
+    // the CTA that processed it, so it is the part most likely still in L2.
+    return ring_stream(s, ring, a.trow + off, res ? a.drow + off : nullptr, len, true,
                        [&](int k, uint32_t stage) {
 #pragma unroll
                          for (int v = 0; v < kVPT; ++v) {
@@ -723,24 +757,12 @@ template <int DT, bool VEC>
 __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned char* ring, int b,
                                             int t0, int d0, int K, bool greedy) {
   const int tid = threadIdx.x;
-  if (tid == 0) {
-    __threadfence();
-    int stop = K;
-    for (int i = 0; i < K; ++i) {
-      if (__ldcg(&P.rows[t0 + i].accept) == 0u) {
-        stop = i;
-        break;
-      }
-    }
-    s.stop = stop;
-  }
-  __syncthreads();
-  const int stop = s.stop;
+  const int stop = s.stop;  // set by the row that decided it
+  if (tid == 0) __threadfence();
   for (int j = tid; j < stop; j += kThreads) P.out_tokens[t0 + j] = P.draft_tokens[d0 + j];
   const int srow = t0 + stop;
   if (tid == 0) {
     P.out_len[b] = stop + 1;
-    P.req_done[b] = 0u;
     atomicAdd(&P.ws->committed, 1u);
   }
   if (greedy) {
@@ -774,8 +796,7 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
     int nparts = (nchunks + kPartChunks - 1) / kPartChunks;
     nparts = nparts > kMaxParts ? kMaxParts : nparts;
     s.slot = -1;
-    if (nparts > 1 && ld_relaxed_gpu(&P.ws->next_item) + kPublishWaves * gridDim.x >=
-                          (unsigned)(P.cu[P.B] + P.B)) {
+    if (nparts > 1 && ld_relaxed_gpu(&P.ws->next_item) + kPublishWaves * gridDim.x >= s.n_items) {
       const unsigned slot = atomicAdd(&P.ws->n_draws, 1u);
       if (slot < (unsigned)P.n_slots) {
         DrawDesc* d = &P.descs[slot];
@@ -831,58 +852,80 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
   return true;
 }
 
-// One row. Returns false if a bulk copy timed out.
+__device__ __forceinline__ int t0_of(const Params& P, int b) { return P.cu[b] + b; }
+
+// Request progress. With K <= kMaxTrackedK draft slots the word holds one
+// "done" bit per target row (bits 0..K) and one "accepted" bit per draft
+// slot (bits 32..32+K-1), so the stop slot is known as soon as the rows up to
+// it are done -- later rows may still be streaming. With more slots it
+// counts finished rows and the request commits when all are done.
+constexpr int kMaxTrackedK = 31;
+
+// Stop slot decided by a progress word (tracked requests), or -1.
+__device__ __forceinline__ int stop_from_state(unsigned long long st, int K) {
+  for (int i = 0; i < K; ++i) {
+    if (!((st >> i) & 1ull)) return -1;         // slot i not decided yet
+    if (!((st >> (32 + i)) & 1ull)) return i;   // first rejection
+  }
+  return ((st >> K) & 1ull) ? K : -1;           // all accepted: needs the bonus row
+}
+
+// Row metadata of target row t into shared memory (thread 0).
+__device__ __noinline__ void row_meta(const Params& P, Smem& s, int t) {
+  const int b = find_request(P.cu, P.B, t);
+  const int t0 = P.cu[b] + b, d0 = P.cu[b];
+  const int K = P.cu[b + 1] - d0;
+  const int i = t - t0;
+  int greedy = P.greedy_all;
+  if (!greedy && P.mode) {
+    const uint8_t m = P.mode[b];
+    if (m == SV_MODE_GREEDY)
+      greedy = 1;
+    else if (m != SV_MODE_SAMPLE && i == 0)
+      atomicOr(&P.ws->status, SV_DATA_BAD_MODE);
+  }
+  int xhat = -1;
+  if (i < K) {
+    xhat = P.draft_tokens[d0 + i];
+    if (xhat < 0 || xhat >= P.V) {
+      atomicOr(&P.ws->status, SV_DATA_BAD_TOKEN);
+      xhat = -1;
+    }
+  }
+  s.b = b;
+  s.t0 = t0;
+  s.d0 = d0;
+  s.K = K;
+  s.i = i;
+  s.greedy = greedy;
+  s.xhat = xhat;
+}
+
+// Statistics of chunks [c0, c1) of a row (and its paired draft row): the
+// online softmax (sampled rows) or the argmax (greedy rows), combined over
+// the CTA into `st` (valid in thread 0). Returns false on a copy timeout.
 template <int DT, bool VEC>
-__device__ bool process_row(const Params& P, Smem& s, unsigned char* ring, int t) {
+__device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const char* trow,
+                            const char* drow, bool greedy, int c0, int c1, PartRec& st) {
   constexpr int EPV = Elem<DT>::kEPV;
   constexpr int CH = kChunkBytes / Elem<DT>::kBytes;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    const int b = find_request(P.cu, P.B, t);
-    const int t0 = P.cu[b] + b, d0 = P.cu[b];
-    const int K = P.cu[b + 1] - d0;
-    const int i = t - t0;
-    int greedy = P.greedy_all;
-    if (!greedy && P.mode) {
-      const uint8_t m = P.mode[b];
-      if (m == SV_MODE_GREEDY)
-        greedy = 1;
-      else if (m != SV_MODE_SAMPLE && i == 0)
-        atomicOr(&P.ws->status, SV_DATA_BAD_MODE);
-    }
-    int xhat = -1;
-    if (i < K) {
-      xhat = P.draft_tokens[d0 + i];
-      if (xhat < 0 || xhat >= P.V) {
-        atomicOr(&P.ws->status, SV_DATA_BAD_TOKEN);
-        xhat = -1;
-      }
-    }
-    s.b = b;
-    s.t0 = t0;
-    s.d0 = d0;
-    s.K = K;
-    s.i = i;
-    s.greedy = greedy;
-    s.xhat = xhat;
-  }
-  __syncthreads();
-  const int b = s.b, t0 = s.t0, d0 = s.d0, K = s.K, i = s.i, xhat = s.xhat;
-  const bool greedy = s.greedy != 0;
   const int V = P.V;
   const size_t rowb = (size_t)V * Elem<DT>::kBytes;
-  const char* trow = static_cast<const char*>(P.target) + (size_t)t * rowb;
+  const size_t off = (size_t)c0 * kChunkBytes;
+  const size_t end = (size_t)c1 * kChunkBytes < rowb ? (size_t)c1 * kChunkBytes : rowb;
+  const size_t len = end > off ? end - off : 0;
+  const int x0 = c0 * CH;  // first element of the slice
   bool ok = true;
-  RowRec rec;
   if (greedy) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     if constexpr (VEC) {
-      ok = ring_stream(s, ring, trow, nullptr, rowb, [&](int k, uint32_t stage) {
+      ok = ring_stream(s, ring, trow + off, nullptr, len, false, [&](int k, uint32_t stage) {
 #pragma unroll
         for (int v = 0; v < kVPT; ++v) {
           const int vi = v * kThreads + tid;
-          const int x = k * CH + vi * EPV;
+          const int x = x0 + k * CH + vi * EPV;
           if (x < V) {
             float f[EPV];
             Elem<DT>::unpack(lds16(stage + 16u * vi), f);
@@ -909,30 +952,25 @@ __device__ bool process_row(const Params& P, Smem& s, unsigned char* ring, int t
       int ix = lane < kWarps ? s.redi[lane] : 0x7fffffff;
       warp_argmax(v, ix);
       if (lane == 0) {
-        const int am = (ix == 0x7fffffff) ? 0 : ix;  // all -inf: index 0, like argmax
-        rec.mc_p = rec.mc_q = 0.f;
-        rec.S_p = rec.S_q = 0.0;
-        rec.argmax = am;
-        rec.accept = (i < K && xhat == am) ? 1u : 0u;
-        if (P.out_probs && i < K) {
-          P.out_probs[2 * (size_t)t] = -1.f;
-          P.out_probs[2 * (size_t)t + 1] = -1.f;
-        }
+        st.mc_p = st.mc_q = 0.f;
+        st.S_p = st.S_q = 0.0;
+        st.amax_v = v;
+        st.amax_i = ix;
       }
     }
   } else {
-    const bool has_d = (i < K) && (P.draft != nullptr);
-    const char* drow = has_d ? static_cast<const char*>(P.draft) + (size_t)(d0 + i) * rowb : nullptr;
     SoftAcc<EPV> at, ad;
     at.init();
     ad.init();
+    const bool has_d = drow != nullptr;
     if constexpr (VEC) {
-      ok = ring_stream(s, ring, trow, drow, rowb, [&](int k, uint32_t stage) {
+      ok = ring_stream(s, ring, trow + off, has_d ? drow + off : nullptr, len, false,
+                       [&](int k, uint32_t stage) {
         float f[kVPT][EPV];
 #pragma unroll
         for (int v = 0; v < kVPT; ++v) {
           const int vi = v * kThreads + tid;
-          if (k * CH + vi * EPV < V) {
+          if (x0 + k * CH + vi * EPV < V) {
             Elem<DT>::unpack(lds16(stage + 16u * vi), f[v]);
           } else {
 #pragma unroll
@@ -944,7 +982,7 @@ __device__ bool process_row(const Params& P, Smem& s, unsigned char* ring, int t
 #pragma unroll
           for (int v = 0; v < kVPT; ++v) {
             const int vi = v * kThreads + tid;
-            if (k * CH + vi * EPV < V) {
+            if (x0 + k * CH + vi * EPV < V) {
               Elem<DT>::unpack(lds16(stage + kChunkBytes + 16u * vi), f[v]);
             } else {
 #pragma unroll
@@ -964,53 +1002,180 @@ __device__ bool process_row(const Params& P, Smem& s, unsigned char* ring, int t
     double Sp, Sq;
     combine_softmax<EPV>(at, ad, has_d, P.c, s, mcp, Sp, mcq, Sq);
     if (tid == 0) {
-      rec.mc_p = mcp;
-      rec.mc_q = mcq;
-      rec.S_p = Sp;
-      rec.S_q = Sq;
-      rec.argmax = 0;
-      rec.accept = 1u;
-      if (!(Sp > 0.0) || (has_d && !(Sq > 0.0))) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
-      if (i < K) {
-        float ph = -1.f, qh = -1.f;
-        unsigned acc = 0u;
-        if (xhat >= 0) {
-          // p(x̂) = 2^(z c - mc_p) / S_p, and min(1, p/q) with q from the
-          // draft row or q = 1 for a one-hot proposal.
-          const float zp = Elem<DT>::scalar(trow, xhat);
-          const float ap = fmaf(zp, P.c, -mcp);
-          const double pd = (double)exp2f(ap) / Sp;
-          double rho;
-          double qd = 1.0;
-          if (has_d) {
-            const float zq = Elem<DT>::scalar(drow, xhat);
-            const float aq = fmaf(zq, P.c, -mcq);
-            qd = (double)exp2f(aq) / Sq;
-            rho = (zq == -INFINITY) ? 0.0 : fmin(1.0, (double)exp2f(ap - aq) * (Sq / Sp));
-          } else {
-            rho = fmin(1.0, pd);
-          }
-          const double u = (double)__ldg(&P.uniforms[2 * (size_t)t]);
-          acc = (u < rho) ? 1u : 0u;
-          ph = (float)pd;
-          qh = (float)qd;
+      st.mc_p = mcp;
+      st.mc_q = mcq;
+      st.S_p = Sp;
+      st.S_q = Sq;
+      st.amax_v = -INFINITY;
+      st.amax_i = 0x7fffffff;
+    }
+  }
+  return ok;
+}
+
+// Merges the statistics of a split row's parts (thread 0): the largest
+// exponent offset of the parts with mass and the sums rescaled to it in
+// fp64; for greedy rows the largest logit, lowest index among ties.
+__device__ __noinline__ PartRec merge_parts(const PartRec* parts, int n) {
+  PartRec m;
+  m.mc_p = m.mc_q = 0.f;
+  m.S_p = m.S_q = 0.0;
+  m.amax_v = -INFINITY;
+  m.amax_i = 0x7fffffff;
+  bool have_p = false, have_q = false;
+  for (int r = 0; r < n; ++r) {
+    const float mp = __ldcg(&parts[r].mc_p), mq = __ldcg(&parts[r].mc_q);
+    if (__ldcg(&parts[r].S_p) > 0.0 && (!have_p || mp > m.mc_p)) { m.mc_p = mp; have_p = true; }
+    if (__ldcg(&parts[r].S_q) > 0.0 && (!have_q || mq > m.mc_q)) { m.mc_q = mq; have_q = true; }
+    float v = __ldcg(&parts[r].amax_v);
+    int ix = __ldcg(&parts[r].amax_i);
+    argmax_merge(m.amax_v, m.amax_i, v, ix);
+  }
+  for (int r = 0; r < n; ++r) {
+    const double sp = __ldcg(&parts[r].S_p), sq = __ldcg(&parts[r].S_q);
+    if (sp > 0.0) m.S_p += sp * exp2((double)__ldcg(&parts[r].mc_p) - (double)m.mc_p);
+    if (sq > 0.0) m.S_q += sq * exp2((double)__ldcg(&parts[r].mc_q) - (double)m.mc_q);
+  }
+  return m;
+}
+
+// Decision for row t from its statistics (thread 0): the row record, the
+// slot's (p(x̂), q(x̂)), and whether this row completes its request.
+template <int DT>
+__device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const PartRec& st) {
+  const int b = s.b, d0 = s.d0, K = s.K, i = s.i, xhat = s.xhat;
+  const bool greedy = s.greedy != 0;
+  const size_t rowb = (size_t)P.V * Elem<DT>::kBytes;
+  const char* trow = static_cast<const char*>(P.target) + (size_t)t * rowb;
+  const bool has_d = !greedy && i < K && P.draft != nullptr;
+  const char* drow = has_d ? static_cast<const char*>(P.draft) + (size_t)(d0 + i) * rowb : nullptr;
+  RowRec rec;
+  if (greedy) {
+    const int am = (st.amax_i == 0x7fffffff) ? 0 : st.amax_i;  // all -inf: index 0, like argmax
+    rec.mc_p = rec.mc_q = 0.f;
+    rec.S_p = rec.S_q = 0.0;
+    rec.argmax = am;
+    rec.accept = (i < K && xhat == am) ? 1u : 0u;
+    if (P.out_probs && i < K) {
+      P.out_probs[2 * (size_t)t] = -1.f;
+      P.out_probs[2 * (size_t)t + 1] = -1.f;
+    }
+  } else {
+    const float mcp = st.mc_p, mcq = st.mc_q;
+    const double Sp = st.S_p, Sq = st.S_q;
+    rec.mc_p = mcp;
+    rec.mc_q = mcq;
+    rec.S_p = Sp;
+    rec.S_q = Sq;
+    rec.argmax = 0;
+    rec.accept = 1u;
+    if (!(Sp > 0.0) || (has_d && !(Sq > 0.0))) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
+    if (i < K) {
+      float ph = -1.f, qh = -1.f;
+      unsigned acc = 0u;
+      if (xhat >= 0) {
+        // p(x̂) = 2^(z c - mc_p) / S_p, and min(1, p/q) with q from the
+        // draft row or q = 1 for a one-hot proposal.
+        const float zp = Elem<DT>::scalar(trow, xhat);
+        const float ap = fmaf(zp, P.c, -mcp);
+        const double pd = (double)exp2f(ap) / Sp;
+        double rho;
+        double qd = 1.0;
+        if (has_d) {
+          const float zq = Elem<DT>::scalar(drow, xhat);
+          const float aq = fmaf(zq, P.c, -mcq);
+          qd = (double)exp2f(aq) / Sq;
+          rho = (zq == -INFINITY) ? 0.0 : fmin(1.0, (double)exp2f(ap - aq) * (Sq / Sp));
+        } else {
+          rho = fmin(1.0, pd);
         }
-        rec.accept = acc;
-        if (P.out_probs) {
-          P.out_probs[2 * (size_t)t] = ph;
-          P.out_probs[2 * (size_t)t + 1] = qh;
-        }
+        const double u = (double)__ldg(&P.uniforms[2 * (size_t)t]);
+        acc = (u < rho) ? 1u : 0u;
+        ph = (float)pd;
+        qh = (float)qd;
+      }
+      rec.accept = acc;
+      if (P.out_probs) {
+        P.out_probs[2 * (size_t)t] = ph;
+        P.out_probs[2 * (size_t)t + 1] = qh;
       }
     }
   }
-  if (!ok) return false;
-  if (tid == 0) {
-    P.rows[t] = rec;
-    __threadfence();
-    const unsigned old = atomicAdd(&P.req_done[b], 1u);
-    s.last = (old == (unsigned)K) ? 1 : 0;
+  P.rows[t] = rec;
+  __threadfence();
+  // s.last: this row makes the request's stop slot known (commit here);
+  // s.stop: that slot.
+  s.last = 0;
+  if (K <= kMaxTrackedK) {
+    const unsigned long long add = (1ull << i) | (rec.accept && i < K ? 1ull << (32 + i) : 0ull);
+    const unsigned long long old = atomicOr(&P.req_state[b], add);
+    const unsigned long long now = old | add;
+    const int stop = stop_from_state(now, K);
+    if (stop >= 0 && stop_from_state(old, K) < 0) {
+      s.last = 1;
+      s.stop = stop;
+    }
+    const unsigned long long all = (K + 1 == 64) ? ~0ull : ((1ull << (K + 1)) - 1ull);
+    if ((now & all) == all) P.req_state[b] = 0ull;  // every row is in: reset for the next call
+  } else {
+    const unsigned long long old = atomicAdd(&P.req_state[b], 1ull);
+    if (old == (unsigned long long)K) {
+      __threadfence();
+      int stop = K;
+      for (int j = 0; j < K; ++j)
+        if (__ldcg(&P.rows[t0_of(P, b) + j].accept) == 0u) {
+          stop = j;
+          break;
+        }
+      s.last = 1;
+      s.stop = stop;
+      P.req_state[b] = 0ull;
+    }
   }
+}
+
+// One work item: a whole row (part < 0) or part `part` of split row t, whose
+// index among the split rows is `split`. Returns false on a copy timeout.
+template <int DT, bool VEC>
+__device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int t, int part,
+                             int split) {
+  const int tid = threadIdx.x;
+  if (tid == 0) row_meta(P, s, t);
   __syncthreads();
+  const int b = s.b, t0 = s.t0, d0 = s.d0, K = s.K, i = s.i;
+  const bool greedy = s.greedy != 0;
+  const size_t rowb = (size_t)P.V * Elem<DT>::kBytes;
+  const char* trow = static_cast<const char*>(P.target) + (size_t)t * rowb;
+  const bool has_d = !greedy && i < K && P.draft != nullptr;
+  const char* drow = has_d ? static_cast<const char*>(P.draft) + (size_t)(d0 + i) * rowb : nullptr;
+  const int nch = (int)((rowb + kChunkBytes - 1) / kChunkBytes);
+  int c0 = 0, c1 = nch;
+  const int np = (int)s.row_parts;
+  if (part >= 0) {
+    const int cpp = (nch + np - 1) / np;
+    c0 = min(nch, part * cpp);
+    c1 = min(nch, c0 + cpp);
+  }
+  PartRec st;
+  if (!slice_stats<DT, VEC>(P, s, ring, trow, drow, greedy, c0, c1, st)) return false;
+  if (part >= 0) {
+    if (tid == 0) {
+      P.parts[(size_t)split * np + part] = st;
+      __threadfence();
+      const unsigned old = atomicAdd(&P.part_done[split], 1u);
+      s.merge = (old == (unsigned)np - 1u) ? 1 : 0;  // this CTA merges the row
+      if (s.merge) {
+        __threadfence();
+        st = merge_parts(P.parts + (size_t)split * np, np);
+        P.part_done[split] = 0u;
+      }
+    }
+    __syncthreads();
+    if (!s.merge) return true;
+  }
+  if (tid == 0) decide_row<DT>(P, s, t, st);
+  __syncthreads();
+  bool ok = true;
   if (s.last) ok = commit_request<DT, VEC>(P, s, ring, b, t0, d0, K, greedy);
   __syncthreads();
   return ok;
@@ -1043,13 +1208,31 @@ __global__ void __launch_bounds__(kThreads, SV_MINBLOCKS) verify_kernel(Params P
     return;
   }
   const unsigned R_t = (unsigned)(P.cu[P.B] + P.B);
+  if (tid == 0) {
+    // Work items: whole rows, then the last rows split into parts.
+    unsigned W = 0, np = 1;
+    if (VEC) {
+      W = min(R_t, min(kTailWaves * gridDim.x, kMaxTailRows));
+      np = kRowParts;
+      if (R_t < gridDim.x) np = max(np, gridDim.x / R_t);  // few rows: spread each row out
+      const unsigned nch = (unsigned)(((size_t)P.V * Elem<DT>::kBytes + kChunkBytes - 1) / kChunkBytes);
+      np = min(np, min(kMaxRowParts, nch));
+      if (W > 0) np = min(np, kMaxPartRecs / W);
+      if (np < 2) W = 0, np = 1;
+    }
+    s.row_parts = np;
+    s.r_full = R_t - W;
+    s.n_items = (R_t - W) + W * np;
+  }
+  __syncthreads();
+  const unsigned n_items = s.n_items, r_full = s.r_full, row_parts = s.row_parts;
   for (;;) {
     if (tid == 0) {
       // Rows first; once they are all handed out, parts of published draws.
       int slot = -1, part = -1;
       const unsigned t = atomicAdd(&P.ws->next_item, 1u);
       s.wk = 0;
-      if (t < R_t) {
+      if (t < n_items) {
         s.wk = 2;
         s.item = (int)t;
       } else {
@@ -1072,8 +1255,16 @@ __global__ void __launch_bounds__(kThreads, SV_MINBLOCKS) verify_kernel(Params P
     const int wk = s.wk, item = s.item, slot = s.slot, part = s.part;
     __syncthreads();
     if (wk == 0) break;
-    const bool ok = wk == 2 ? process_row<DT, VEC>(P, s, ring, item)
-                            : draw_part<DT, VEC>(P, s, ring, slot, part);
+    bool ok;
+    if (wk == 1) {
+      ok = draw_part<DT, VEC>(P, s, ring, slot, part);
+    } else if ((unsigned)item < r_full) {
+      ok = process_item<DT, VEC>(P, s, ring, item, -1, 0);
+    } else {
+      const unsigned j = (unsigned)item - r_full;
+      ok = process_item<DT, VEC>(P, s, ring, (int)(r_full + j / row_parts), (int)(j % row_parts),
+                                 (int)(j / row_parts));
+    }
     if (!ok) {
       // A bulk copy never completed: report it and leave without touching
       // the shared counters (the workspace must be zero-filled again).
@@ -1115,19 +1306,22 @@ static size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 static int n_draw_slots(long long B) { return (int)(B < kMaxDrawSlots ? B : kMaxDrawSlots); }
 static int tsum_stride(int V) { return (V + kThreads * 4 - 1) / (kThreads * 4); }
 
-// header | req_done[B] | slot_state[S] | descs[S] | tsum[S][stride] | rows[R_t]
+// header | req_state[B] | slot_state[S] | descs[S] | tsum[S][stride] |
+// part_done[kMaxTailRows] | parts[kMaxPartRecs] | rows[R_t]
 struct WsLayout {
-  size_t req_done, slot_state, descs, tsum, rows;
+  size_t req_done, slot_state, descs, tsum, part_done, parts, rows;
 };
 
 static WsLayout ws_layout(long long B, int V) {
   const size_t S = (size_t)n_draw_slots(B);
   WsLayout L;
   L.req_done = sizeof(WsHeader);
-  L.slot_state = L.req_done + align16((size_t)B * sizeof(unsigned));
+  L.slot_state = L.req_done + align16((size_t)B * sizeof(unsigned long long));
   L.descs = L.slot_state + align16(S * sizeof(unsigned));
   L.tsum = L.descs + S * sizeof(DrawDesc);
-  L.rows = L.tsum + align16(S * (size_t)tsum_stride(V) * sizeof(double));
+  L.part_done = L.tsum + align16(S * (size_t)tsum_stride(V) * sizeof(double));
+  L.parts = L.part_done + align16((size_t)kMaxTailRows * sizeof(unsigned));
+  L.rows = L.parts + (size_t)kMaxPartRecs * sizeof(PartRec);
   return L;
 }
 
@@ -1172,8 +1366,9 @@ static cudaError_t launch(const Params& P, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   e = resident_ctas<DT, VEC>(dev, &resident);
   if (e != cudaSuccess) return e;
+  // At most one CTA per possible work item (rows may be split into parts).
   long long grid = resident;
-  if (grid > P.row_cap) grid = P.row_cap;
+  if (grid > P.row_cap * (long long)kMaxRowParts) grid = P.row_cap * (long long)kMaxRowParts;
   if (grid < 1) grid = 1;
   verify_kernel<DT, VEC><<<(unsigned)grid, kThreads, dyn_smem<VEC>(), st>>>(P);
   return cudaGetLastError();
@@ -1217,11 +1412,13 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
   P.out_len = out_len;
   P.out_probs = greedy_all ? nullptr : out_probs;
   P.ws = reinterpret_cast<WsHeader*>(ws);
-  P.req_done = reinterpret_cast<unsigned*>(ws + L.req_done);
+  P.req_state = reinterpret_cast<unsigned long long*>(ws + L.req_done);
   P.slot_state = reinterpret_cast<unsigned*>(ws + L.slot_state);
   P.descs = reinterpret_cast<DrawDesc*>(ws + L.descs);
   P.tsum = reinterpret_cast<double*>(ws + L.tsum);
   P.n_slots = n_draw_slots(B);
+  P.part_done = reinterpret_cast<unsigned*>(ws + L.part_done);
+  P.parts = reinterpret_cast<PartRec*>(ws + L.parts);
   P.tsum_stride = tsum_stride(V);
   P.rows = reinterpret_cast<RowRec*>(ws + L.rows);
   P.row_cap = (long long)((workspace_bytes - L.rows) / sizeof(RowRec));

@@ -34,7 +34,8 @@ def test_workspace_size(lib):
     for B, R, V in [(1, 5, 32000), (64, 384, 128256), (256, 2048, 151936), (513, 3000, 256000), (7, 9, 1)]:
         S = min(B, 4096)            # draw slots
         tiles = (V + 1023) // 1024  # tile sums per slot (fp32-sized tiles)
-        want = 64 + a16(4 * B) + a16(4 * S) + 64 * S + a16(8 * S * tiles) + 32 * R
+        split = a16(4 * 4096) + 32 * 16384  # counters and records of split rows
+        want = 64 + a16(8 * B) + a16(4 * S) + 64 * S + a16(8 * S * tiles) + split + 32 * R
         assert api.spec_verify_workspace_size(B, R, V) == want
     assert lib.spec_verify_workspace_size(-1, 4, 10) == 0
     assert lib.spec_verify_workspace_size(4, 4, 0) == 0
