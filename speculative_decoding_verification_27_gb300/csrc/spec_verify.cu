@@ -127,6 +127,7 @@ constexpr int max_vocab(int dtype) { return kMaxScanTiles * kThreads * (dtype ==
 constexpr int kStages = SV_STAGES;                  // stages (kStages - 1 in flight)
 constexpr int kVPT = SV_VPT;                        // 16-byte vectors per thread per chunk
 constexpr int kChunkBytes = kThreads * 16 * kVPT;   // bytes of one row per stage
+static_assert((kVPT & (kVPT - 1)) == 0, "vectors per thread must be a power of two");
 constexpr int kStageBytes = 2 * kChunkBytes;        // target + draft chunk
 constexpr int kRingBytes = kStages * kStageBytes;   // dynamic shared memory per CTA
 constexpr int kPartChunks = SV_PART_CHUNKS;         // ring chunks per draw part
@@ -198,57 +199,143 @@ struct Smem {
   float wtot[kMaxScanTiles * kWarps];
 };
 
+// Raw 16-byte vectors of logits as the ring holds them: the all -inf vector,
+// the elements as fp32 pairs (lanes 2i, 2i+1) and the maximum over N vectors.
+template <int DT>
+struct Raw;
+
+template <>
+struct Raw<0> {
+  static constexpr uint32_t kNegInf = 0xff800000u;
+  __device__ __forceinline__ static void pairs(const uint4& v, f2_t (&z)[2]) {
+    z[0] = f2_pack(__uint_as_float(v.x), __uint_as_float(v.y));
+    z[1] = f2_pack(__uint_as_float(v.z), __uint_as_float(v.w));
+  }
+  template <int N>
+  __device__ __forceinline__ static float max_of(const uint4 (&v)[N]) {
+    float t[4 * N];
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+      t[4 * u] = __uint_as_float(v[u].x);
+      t[4 * u + 1] = __uint_as_float(v[u].y);
+      t[4 * u + 2] = __uint_as_float(v[u].z);
+      t[4 * u + 3] = __uint_as_float(v[u].w);
+    }
+#pragma unroll
+    for (int w = 2 * N; w >= 1; w /= 2)
+#pragma unroll
+      for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+    return t[0];
+  }
+};
+
+template <>
+struct Raw<1> {
+  static constexpr uint32_t kNegInf = 0xff80ff80u;
+  // bf16 is the top half of an fp32: the low element of a word is shifted
+  // up, the high one masked.
+  __device__ __forceinline__ static void pairs(const uint4& v, f2_t (&z)[4]) {
+    z[0] = f2_pack(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+    z[1] = f2_pack(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+    z[2] = f2_pack(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
+    z[3] = f2_pack(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+  }
+  // Pairwise bf16x2 maxima down to one word, then its two halves.
+  template <int N>
+  __device__ __forceinline__ static float max_of(const uint4 (&v)[N]) {
+    uint32_t t[4 * N];
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+      t[4 * u] = v[u].x;
+      t[4 * u + 1] = v[u].y;
+      t[4 * u + 2] = v[u].z;
+      t[4 * u + 3] = v[u].w;
+    }
+#pragma unroll
+    for (int w = 2 * N; w >= 1; w /= 2)
+#pragma unroll
+      for (int j = 0; j < w; ++j) t[j] = bf2_max(t[j], t[j + w]);
+    return fmaxf(__uint_as_float(t[0] << 16), __uint_as_float(t[0] & 0xffff0000u));
+  }
+};
+
 // Online softmax state of one thread: running maximum m, its fp32 exponent
 // offset mc = fp32(m * c) (0 while m is -inf) and one partial sum per lane of
-// the 16-byte vector. Every term is 2^(z c - mc).
+// the 16-byte vector, kept as fp32 pairs. Every term is 2^(z c - mc).
 template <int EPV>
 struct SoftAcc {
+  static constexpr int kPairs = EPV / 2;
   float m, mc;
-  float a[EPV];
+  f2_t a[kPairs];
   __device__ __forceinline__ void init() {
     m = -INFINITY;
     mc = 0.f;
 #pragma unroll
-    for (int j = 0; j < EPV; ++j) a[j] = 0.f;
+    for (int i = 0; i < kPairs; ++i) a[i] = 0ull;  // two +0.0f
+  }
+  __device__ __forceinline__ float lane(int j) const {
+    float lo, hi;
+    f2_unpack(a[j >> 1], lo, hi);
+    return (j & 1) ? hi : lo;
   }
   // Raises the running maximum to vm (if larger), rescaling the partial sums.
   __device__ __forceinline__ void raise(float vm, float c) {
     if (vm > m) {
       float nmc = __fmul_rn(vm, c);
-      float s = (m == -INFINITY) ? 0.f : ex2(mc - nmc);
+      const f2_t s = f2_splat((m == -INFINITY) ? 0.f : ex2(mc - nmc));
 #pragma unroll
-      for (int j = 0; j < EPV; ++j) a[j] *= s;
+      for (int i = 0; i < kPairs; ++i) a[i] = f2_mul(a[i], s);
       m = vm;
       mc = nmc;
     }
+  }
+  __device__ __forceinline__ void accumulate(const f2_t (&z)[kPairs], f2_t cc, f2_t nmc) {
+#pragma unroll
+    for (int i = 0; i < kPairs; ++i) a[i] = f2_add(a[i], f2_ex2(f2_fma(z[i], cc, nmc)));
   }
   __device__ __forceinline__ void add(const float (&f)[EPV], float c) {
     float vm = f[0];
 #pragma unroll
     for (int j = 1; j < EPV; ++j) vm = fmaxf(vm, f[j]);
     raise(vm, c);
+    f2_t z[kPairs];
 #pragma unroll
-    for (int j = 0; j < EPV; ++j) a[j] += ex2(fmaf(f[j], c, -mc));
+    for (int i = 0; i < kPairs; ++i) z[i] = f2_pack(f[2 * i], f[2 * i + 1]);
+    accumulate(z, f2_splat(c), f2_splat(-mc));
   }
-  // N vectors at once: one maximum (a shallow tree) and one rescale check.
-  template <int N>
-  __device__ __forceinline__ void add_n(const float (&f)[N][EPV], float c) {
-    float t[N * EPV];
+  // N raw vectors at once: one maximum and one rescale check.
+  template <int DT, int N>
+  __device__ __forceinline__ void add_raw(const uint4 (&v)[N], float c) {
+    raise(Raw<DT>::template max_of<N>(v), c);
+    const f2_t cc = f2_splat(c), nmc = f2_splat(-mc);
 #pragma unroll
-    for (int u = 0; u < N; ++u)
-#pragma unroll
-      for (int j = 0; j < EPV; ++j) t[u * EPV + j] = f[u][j];
-#pragma unroll
-    for (int w = (N * EPV) / 2; w >= 1; w /= 2)
-#pragma unroll
-      for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
-    raise(t[0], c);
-#pragma unroll
-    for (int u = 0; u < N; ++u)
-#pragma unroll
-      for (int j = 0; j < EPV; ++j) a[j] += ex2(fmaf(f[u][j], c, -mc));
+    for (int u = 0; u < N; ++u) {
+      f2_t z[kPairs];
+      Raw<DT>::pairs(v[u], z);
+      accumulate(z, cc, nmc);
+    }
   }
 };
+
+// The kVPT vectors this thread consumes from a ring stage holding elements
+// [x, x + kVPT * kThreads * EPV) of a row: whole vectors inside the row are
+// read, those at or past V read as -inf.
+template <int DT>
+__device__ __forceinline__ void stage_vectors(uint32_t stage, int x, int V, uint4 (&rv)[kVPT]) {
+  constexpr int EPV = Elem<DT>::kEPV;
+  const int tid = threadIdx.x;
+  if (x + kVPT * kThreads * EPV <= V) {
+#pragma unroll
+    for (int v = 0; v < kVPT; ++v) rv[v] = lds16(stage + 16u * (v * kThreads + tid));
+  } else {
+    const uint32_t n = Raw<DT>::kNegInf;
+#pragma unroll
+    for (int v = 0; v < kVPT; ++v) {
+      const int vi = v * kThreads + tid;
+      rv[v] = (x + vi * EPV < V) ? lds16(stage + 16u * vi) : make_uint4(n, n, n, n);
+    }
+  }
+}
 
 // ---------------------------------------------------------------------------
 // Bulk-copy ring
@@ -392,12 +479,12 @@ __device__ void combine_softmax(SoftAcc<EPV>& at, SoftAcc<EPV>& ad, bool has_d, 
   const float mcq = (Mq == -INFINITY) ? 0.f : __fmul_rn(Mq, c);
   DF tp{0.f, 0.f}, tq{0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < EPV; ++j) tp = df_add_f(tp, at.a[j]);
+  for (int j = 0; j < EPV; ++j) tp = df_add_f(tp, at.lane(j));
   tp = df_mul_f(tp, (at.m == -INFINITY) ? 0.f : ex2(at.mc - mcp));
   tp = warp_sum_df(tp);
   if (has_d) {
 #pragma unroll
-    for (int j = 0; j < EPV; ++j) tq = df_add_f(tq, ad.a[j]);
+    for (int j = 0; j < EPV; ++j) tq = df_add_f(tq, ad.lane(j));
     tq = df_mul_f(tq, (ad.m == -INFINITY) ? 0.f : ex2(ad.mc - mcq));
     tq = warp_sum_df(tq);
   }
@@ -922,20 +1009,23 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
     int bi = 0x7fffffff;
     if constexpr (VEC) {
       ok = ring_stream(s, ring, trow + off, nullptr, len, false, [&](int k, uint32_t stage) {
+        uint4 rv[kVPT];
+        stage_vectors<DT>(stage, x0 + k * CH, V, rv);
+        const float cm = Raw<DT>::template max_of<kVPT>(rv);
+        if (cm > bv) {
+          // A new maximum: its first occurrence in this thread's elements,
+          // which it visits in increasing index order.
+          int first = 0x7fffffff;
 #pragma unroll
-        for (int v = 0; v < kVPT; ++v) {
-          const int vi = v * kThreads + tid;
-          const int x = x0 + k * CH + vi * EPV;
-          if (x < V) {
+          for (int v = kVPT - 1; v >= 0; --v) {
             float f[EPV];
-            Elem<DT>::unpack(lds16(stage + 16u * vi), f);
+            Elem<DT>::unpack(rv[v], f);
 #pragma unroll
-            for (int j = 0; j < EPV; ++j)
-              if (f[j] > bv) {
-                bv = f[j];
-                bi = x + j;
-              }
+            for (int j = EPV - 1; j >= 0; --j)
+              if (f[j] == cm) first = x0 + k * CH + (v * kThreads + tid) * EPV + j;
           }
+          bv = cm;
+          bi = first;
         }
       });
     } else {
@@ -966,30 +1056,12 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
     if constexpr (VEC) {
       ok = ring_stream(s, ring, trow + off, has_d ? drow + off : nullptr, len, false,
                        [&](int k, uint32_t stage) {
-        float f[kVPT][EPV];
-#pragma unroll
-        for (int v = 0; v < kVPT; ++v) {
-          const int vi = v * kThreads + tid;
-          if (x0 + k * CH + vi * EPV < V) {
-            Elem<DT>::unpack(lds16(stage + 16u * vi), f[v]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < EPV; ++j) f[v][j] = -INFINITY;
-          }
-        }
-        at.add_n<kVPT>(f, P.c);
+        uint4 rv[kVPT];
+        stage_vectors<DT>(stage, x0 + k * CH, V, rv);
+        at.template add_raw<DT, kVPT>(rv, P.c);
         if (has_d) {
-#pragma unroll
-          for (int v = 0; v < kVPT; ++v) {
-            const int vi = v * kThreads + tid;
-            if (x0 + k * CH + vi * EPV < V) {
-              Elem<DT>::unpack(lds16(stage + kChunkBytes + 16u * vi), f[v]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < EPV; ++j) f[v][j] = -INFINITY;
-            }
-          }
-          ad.add_n<kVPT>(f, P.c);
+          stage_vectors<DT>(stage + kChunkBytes, x0 + k * CH, V, rv);
+          ad.template add_raw<DT, kVPT>(rv, P.c);
         }
       });
     } else {

@@ -195,6 +195,49 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Two fp32 lanes in one 64-bit register, for the packed fp32 instructions of
+// sm_100 and later (one instruction, two IEEE round-to-nearest results: each
+// lane is bit-identical to the scalar instruction).
+typedef unsigned long long f2_t;
+
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
+  f2_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_splat(float x) { return f2_pack(x, x); }
+__device__ __forceinline__ void f2_unpack(f2_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+  f2_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+  f2_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+  f2_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_ex2(f2_t v) {
+  float lo, hi;
+  f2_unpack(v, lo, hi);
+  return f2_pack(ex2(lo), ex2(hi));
+}
+
+// Lane-wise maximum of two bf16 pairs (a NaN lane yields the other operand,
+// like fmaxf). Exact, so the fp32 value of the result is the fp32 maximum.
+__device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // Double-float value hi + lo (|lo| <= ulp(hi)/2): error-free transformations
 // keep sums of fp32 partials accurate to ~2^-44 relative without fp64 math.
 struct DF {
