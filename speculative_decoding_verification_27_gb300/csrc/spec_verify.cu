@@ -321,6 +321,14 @@ struct SoftAcc {
 // [x, x + kVPT * kThreads * EPV) of a row: whole vectors inside the row are
 // read, those at or past V read as -inf.
 template <int DT>
+__device__ __forceinline__ uint4 stage_vector(uint32_t stage, int x, int V, int v, bool whole) {
+  constexpr int EPV = Elem<DT>::kEPV;
+  const int vi = v * kThreads + threadIdx.x;
+  const uint32_t n = Raw<DT>::kNegInf;
+  return (whole || x + vi * EPV < V) ? lds16(stage + 16u * vi) : make_uint4(n, n, n, n);
+}
+
+template <int DT>
 __device__ __forceinline__ void stage_vectors(uint32_t stage, int x, int V, uint4 (&rv)[kVPT]) {
   constexpr int EPV = Elem<DT>::kEPV;
   const int tid = threadIdx.x;
@@ -597,26 +605,70 @@ __device__ bool tile_sums(const Params& P, Smem& s, unsigned char* ring, const D
     size_t len = (size_t)ntl * TILE * Elem<DT>::kBytes;
     if (off + len > row_bytes) len = row_bytes - off;
     const bool res = a.kind == kResidual;
+    const bool onehot = a.kind == kOneHot;
+    const f2_t cc = f2_splat(P.c), nmcp = f2_splat(-a.mcp), nmcq = f2_splat(-a.mcq);
+    const f2_t nbhi = f2_splat(-a.bhi), nblo = f2_splat(-a.blo);
+    constexpr int NP = EPV / 2;
     // Last chunk first: the end of the stop row was streamed most recently by
     // the CTA that processed it, so it is the part most likely still in L2.
     return ring_stream(s, ring, a.trow + off, res ? a.drow + off : nullptr, len, true,
                        [&](int k, uint32_t stage) {
+      const int xc = (tile0 + k * kVPT) * TILE;  // first element of the chunk
+      const bool whole = xc + kVPT * TILE <= V;
+      float ts[kVPT];
 #pragma unroll
-                         for (int v = 0; v < kVPT; ++v) {
-                           const int l = k * kVPT + v;
-                           const int vi = v * kThreads + tid;
-                           const int x = (tile0 + l) * TILE + tid * EPV;
-                           float zp[EPV], zq[EPV];
-                           if (x < V) {
-                             Elem<DT>::unpack(lds16(stage + 16u * vi), zp);
-                             if (res) Elem<DT>::unpack(lds16(stage + kChunkBytes + 16u * vi), zq);
-                           } else {
+      for (int v = 0; v < kVPT; ++v) {
+        f2_t zp[NP], acc = 0ull;
+        Raw<DT>::pairs(stage_vector<DT>(stage, xc, V, v, whole), zp);
+        if (res) {
+          f2_t zq[NP];
+          Raw<DT>::pairs(stage_vector<DT>(stage + kChunkBytes, xc, V, v, whole), zq);
 #pragma unroll
-                             for (int j = 0; j < EPV; ++j) zp[j] = zq[j] = -INFINITY;
-                           }
-                           if (l < ntl) one_tile(l, zp, zq);
-                         }
-                       });
+          for (int i = 0; i < NP; ++i) {
+            const f2_t ep = f2_ex2(f2_fma(zp[i], cc, nmcp));
+            const f2_t eq = f2_ex2(f2_fma(zq[i], cc, nmcq));
+            float lo, hi;
+            f2_unpack(f2_fma(eq, nblo, f2_fma(eq, nbhi, ep)), lo, hi);
+            acc = f2_add(acc, f2_pack(fmaxf(lo, 0.f), fmaxf(hi, 0.f)));
+          }
+        } else {
+          const int xv = xc + (v * kThreads + tid) * EPV;
+          const int drop = (onehot && (unsigned)(a.xhat - xv) < (unsigned)EPV) ? a.xhat - xv : -1;
+#pragma unroll
+          for (int i = 0; i < NP; ++i) {
+            f2_t ep = f2_ex2(f2_fma(zp[i], cc, nmcp));
+            if ((drop >> 1) == i) {  // the rejected one-hot proposal has no mass
+              float lo, hi;
+              f2_unpack(ep, lo, hi);
+              ep = (drop & 1) ? f2_pack(lo, 0.f) : f2_pack(0.f, hi);
+            }
+            acc = f2_add(acc, ep);
+          }
+        }
+        float lo, hi;
+        f2_unpack(acc, lo, hi);
+        ts[v] = lo + hi;
+      }
+      // Warp totals of the chunk's kVPT tiles: each halving step trades half
+      // of the tiles with the partner lane, then a plain butterfly; lane
+      // j * (32 / kVPT) ends with the total of tile j.
+      int t = 0;
+#pragma unroll
+      for (int half = kVPT / 2, o = 16; half >= 1; half /= 2, o /= 2) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+          const float send = up ? ts[i] : ts[i + half];
+          const float keep = up ? ts[i + half] : ts[i];
+          ts[i] = keep + __shfl_xor_sync(kFull, send, o);
+        }
+        if (up) t += half;
+      }
+#pragma unroll
+      for (int o = 16 / kVPT; o >= 1; o /= 2) ts[0] += __shfl_xor_sync(kFull, ts[0], o);
+      const int l = k * kVPT + t;
+      if ((lane & (32 / kVPT - 1)) == 0 && l < ntl) s.wtot[l * kWarps + warp] = ts[0];
+    });
   } else {
     for (int l = 0; l < ntl; ++l) {
       const int x = (tile0 + l) * TILE + tid * EPV;
