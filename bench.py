@@ -41,7 +41,9 @@ WORKLOAD = ("sampling verify B=256 K=7 V=151936 bf16 T=0.7, peaked rank-score ro
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per verify launch on this workload from one ncu
 # capture, valid only for the kernel sources whose hash is recorded with it.
-TRAFFIC = {"sources_sha256": None, "bytes_per_launch": None, "profile": None}
+TRAFFIC = {"sources_sha256": "411d282be53444e2c5c1713a2ae1a0b653a233d33cdf9950a79f0443e8d42136",
+           "bytes_per_launch": 1273348000 + 4961024,
+           "profile": "profiles/verify_kernel_sampling_B256_K7_V151936_bf16.md"}
 
 
 def kernel_sources_hash() -> str:
@@ -340,6 +342,7 @@ def run_ours(args):
                        "mean_acceptance_length": committed / B},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+                     "traffic_source": TRAFFIC["profile"] if traffic else None,
                      "kernel": "verify_kernel", "mean_launch_ms": mean_launch_ms,
                      "algorithmic_bytes_per_launch": alg_bytes},
         "e2e": e2e,
