@@ -63,6 +63,23 @@ def measured_peaks():
         return None
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over all ranks (the slowest rank's time); x itself
+    when no process group is running."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank verifies its own batch of the same shape (weak scaling)."""
+    return seed + rank
+
+
 def make_batch(seed: int, B: int = 256):
     from speculative_decoding_verification_27_gb300 import workloads as W
     return W.config3(seed=seed, B=B)
@@ -215,7 +232,7 @@ def run_ours(args):
     build.build_library()
     api.load()
 
-    batch = make_batch(args.seed + rank, args.batch)
+    batch = make_batch(rank_seed(args.seed, rank), args.batch)
     db = parity.to_device(batch)
     B, R_t = batch.B, batch.R_t
     ws = api.new_workspace(B, R_t, batch.V)
@@ -252,11 +269,7 @@ def run_ours(args):
         t_wall = time.perf_counter() - t_wall
     clocks = clk.summary()
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    region_ms = starts[0].elapsed_time(ends[-1])
-    if world > 1:
-        t = torch.tensor([region_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        region_ms = float(t.item())
+    region_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), "cuda")
     ms_per_step = region_ms / args.steps
     mean_launch_ms = float(np.mean(per_launch_ms))
 
@@ -303,11 +316,7 @@ def run_ours(args):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, "cuda")
         e2e = {"value": R_t * world / (e_ms * 1e-3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms, "steps": n_e2e}
 
