@@ -27,7 +27,8 @@
  *
  * Conventions for every entry point:
  *   - Array arguments are DEVICE pointers owned by the caller. The library
- *     allocates no device memory; scratch space is the caller's workspace.
+ *     allocates no device memory; scratch space is the caller's workspace
+ *     (spec_verify_noalloc instead uses a fixed block inside the library).
  *   - Work is enqueued asynchronously on `cuda_stream` (a cudaStream_t; NULL
  *     is the legacy default stream). Results are valid once the stream has
  *     reached that point.
@@ -152,6 +153,55 @@ sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype, int32_t 
                              const int32_t* draft_tokens, const int32_t* cu_draft,
                              int32_t* out_tokens, int32_t* out_len, void* workspace,
                              size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * spec_verify without a caller workspace: the scratch memory lives in a
+ * fixed block that is part of the library's device image, so the call
+ * allocates nothing and takes no workspace argument. The pages have no
+ * counterpart; this is a deployment convenience, not part of the method.
+ *
+ * Who needs it. Some callers cannot hand over a workspace:
+ *   - plain C programs that have no device allocator of their own;
+ *   - serving loops that reserve all device memory when they start and may
+ *     not allocate or free while requests are in flight, where a cudaMalloc
+ *     could fail, or stall the whole device until it completes.
+ * This entry point lets them verify without any allocation, by the library
+ * or by the caller.
+ *
+ * Limit. The fixed block holds SV_NOALLOC_SCRATCH_BYTES (4 MiB). A batch
+ * fits when spec_verify_workspace_size(B, R_t, V) <= SV_NOALLOC_SCRATCH_BYTES
+ * (for example B = 256, K = 7, V = 151936 needs about 0.9 MiB).
+ *   - If B and V alone need more than the block, the call returns
+ *     SV_ERR_INVALID_ARG before anything is enqueued.
+ *   - R_t is known only on the device (cu_draft[B] + B). If the rows do not
+ *     fit, the kernel sets SV_DATA_BAD_OFFSETS in status_out and writes no
+ *     output.
+ *
+ * Arguments, outputs and validation are those of spec_verify, except:
+ *   status_out   optional device pointer to one uint32_t. After the call it
+ *                holds that call's SV_DATA_* / SV_DEV_* bits (0 = clean).
+ *                NULL: the bits are dropped.
+ *
+ * Every call clears the part of the block that must start at zero (the
+ * counters and per-request state) on the stream before the kernel runs, so
+ * a call never inherits state, not even from a call that failed.
+ *
+ * One block per device, shared by all callers on that device:
+ *   - calls on one device must not overlap. Two calls in flight at the same
+ *     time (on different streams, or from different threads without
+ *     ordering) race on the block and both results are undefined.
+ *     Issue them on one stream, or order them yourself;
+ *   - the first call on a device does one-time setup: it looks up the
+ *     block's address and configures the kernel. Make that first call
+ *     outside any stream capture.
+ */
+#define SV_NOALLOC_SCRATCH_BYTES 4194304u /* 4 MiB */
+sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                              int32_t V, int32_t B, const int32_t* draft_tokens,
+                              const int32_t* cu_draft, const uint8_t* mode,
+                              const float* uniforms, float temperature, int32_t* out_tokens,
+                              int32_t* out_len, float* out_probs, uint32_t* status_out,
+                              void* cuda_stream);
 
 /*
  * N-gram / prompt-lookup proposer ("5.2 Draft 模型与无模型方案", §4.1 and §6):

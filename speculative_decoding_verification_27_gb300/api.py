@@ -138,6 +138,36 @@ def spec_verify(target: torch.Tensor, draft: Optional[torch.Tensor], draft_token
     return out_tokens, out_len, out_probs
 
 
+SV_NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def _noalloc_fn():
+    lib = load()
+    fn = lib.spec_verify_noalloc
+    P = ctypes.c_void_p
+    fn.argtypes = [P, P, ctypes.c_int, ctypes.c_int32, ctypes.c_int32, P, P, P, P, ctypes.c_float,
+                   P, P, P, P, P]
+    fn.restype = ctypes.c_int
+    return fn
+
+
+def spec_verify_noalloc(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor,
+                        cu_draft: torch.Tensor, uniforms: torch.Tensor, temperature: float,
+                        mode: Optional[torch.Tensor], out_tokens: torch.Tensor, out_len: torch.Tensor,
+                        out_probs: Optional[torch.Tensor] = None,
+                        status_out: Optional[torch.Tensor] = None, stream=None):
+    """spec_verify on the library's fixed scratch block: no workspace argument
+    and no allocation. Outputs (and the optional one-element int32 status
+    tensor) are the caller's. Calls on one device must not overlap."""
+    B = cu_draft.shape[0] - 1
+    st = _noalloc_fn()(_ptr(target), _ptr(draft), _dtype(target), int(target.shape[1]), int(B),
+                       _ptr(draft_tokens), _ptr(cu_draft), _ptr(mode), _ptr(uniforms),
+                       float(temperature), _ptr(out_tokens), _ptr(out_len), _ptr(out_probs),
+                       _ptr(status_out), _stream(stream))
+    _check("spec_verify_noalloc", st)
+    return out_tokens, out_len, out_probs
+
+
 def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, cu_draft: torch.Tensor, *,
                        out_tokens=None, out_len=None, workspace=None, stream=None):
     """Strict (greedy) verify-and-commit. Returns (out_tokens, out_len)."""

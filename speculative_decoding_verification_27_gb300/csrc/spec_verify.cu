@@ -1560,9 +1560,60 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// Verify without a caller workspace: scratch in a fixed device block
+// ---------------------------------------------------------------------------
+// The block is part of the module image, so using it needs no allocation.
+// Its address is looked up once per device, with that device current.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_SCRATCH_BYTES];
+static std::atomic<void*> g_noalloc_ptr[kMaxDevices];
+
+static cudaError_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  void* p = dev < kMaxDevices ? g_noalloc_ptr[dev].load(std::memory_order_acquire) : nullptr;
+  if (!p) {
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    if (dev < kMaxDevices) g_noalloc_ptr[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return cudaSuccess;
+}
+
 }  // namespace sv
 
 extern "C" {
+
+sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                              int32_t V, int32_t B, const int32_t* draft_tokens,
+                              const int32_t* cu_draft, const uint8_t* mode,
+                              const float* uniforms, float temperature, int32_t* out_tokens,
+                              int32_t* out_len, float* out_probs, uint32_t* status_out,
+                              void* cuda_stream) {
+  if (B < 0 || V < 1 || (status_out && (uintptr_t)status_out % 4)) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!cu_draft) return SV_ERR_INVALID_ARG;
+  // The row count lives on the device; size the check by the largest R_t the
+  // block could hold for this B and V, and let the kernel flag offsets past it.
+  const sv::WsLayout L = sv::ws_layout(B, V);
+  if (L.rows + sizeof(sv::RowRec) > SV_NOALLOC_SCRATCH_BYTES) return SV_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  if (sv::noalloc_scratch(&scratch) != cudaSuccess) return SV_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  // Counters, per-request state, draw slots and split-row counters start at
+  // zero; the per-row records after them are written before they are read.
+  if (cudaMemsetAsync(scratch, 0, L.rows, st) != cudaSuccess) return SV_ERR_CUDA;
+  const sv_status s = sv::run_verify(target_logits, draft_logits, dtype, V, B, draft_tokens,
+                                     cu_draft, mode, uniforms, temperature, out_tokens, out_len,
+                                     out_probs, scratch, SV_NOALLOC_SCRATCH_BYTES, cuda_stream, 0);
+  if (s != SV_OK) return s;
+  if (status_out && cudaMemcpyAsync(status_out, scratch, sizeof(uint32_t),
+                                    cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return SV_OK;
+}
 
 size_t spec_verify_workspace_size(int32_t B, int32_t R_t, int32_t V) {
   if (B < 0 || R_t < 0 || V < 1) return 0;
