@@ -186,6 +186,8 @@ struct Smem {
   int wk, item, slot, part;
   unsigned n_items, r_full, row_parts;  // work-item layout of this launch
   int b, t0, d0, K, i, greedy, xhat, last, stop, merge, pick, pick2, tok;
+  int zx_ok;        // z_p(x̂) (and z_q(x̂)) were taken from the ring during the row pass
+  float zx_p, zx_q, u_acc;
   float redf[kWarps];
   float redf2[kWarps];
   int redi[kWarps];
@@ -343,6 +345,24 @@ __device__ __forceinline__ void stage_vectors(uint32_t stage, int x, int V, uint
       rv[v] = (x + vi * EPV < V) ? lds16(stage + 16u * vi) : make_uint4(n, n, n, n);
     }
   }
+}
+
+// Element j of vector v of rv (run once per row, by one thread).
+template <int DT>
+__device__ __forceinline__ float pick_element(const uint4 (&rv)[kVPT], int v, int j) {
+  constexpr int EPV = Elem<DT>::kEPV;
+  float out = 0.f;
+#pragma unroll
+  for (int u = 0; u < kVPT; ++u) {
+    if (u == v) {
+      float f[EPV];
+      Elem<DT>::unpack(rv[u], f);
+#pragma unroll
+      for (int q = 0; q < EPV; ++q)
+        if (q == j) out = f[q];
+    }
+  }
+  return out;
 }
 
 // ---------------------------------------------------------------------------
@@ -513,6 +533,24 @@ __device__ void combine_softmax(SoftAcc<EPV>& at, SoftAcc<EPV>& ad, bool has_d, 
       S_q = (double)w.hi + (double)w.lo;
     }
   }
+}
+
+// The same search by a whole warp: each round tests 32 evenly spaced
+// candidates of the remaining range at once (cu[b] + b increases with b, so
+// the candidates that pass form a prefix), two rounds up to B = 1024.
+__device__ __forceinline__ int find_request_warp(const int32_t* cu, int B, int t, int lane) {
+  int lo = 0, n = B;  // the answer lies in [lo, lo + n); cu[lo] + lo <= t
+  while (n > 1) {
+    const int step = (n + 31) >> 5;
+    const int c = lo + lane * step;
+    const bool pass = c < lo + n && cu[c] + c <= t;
+    const unsigned m = __ballot_sync(kFull, pass);
+    const int k = 31 - __clz(m);  // lane 0 (candidate lo) always passes
+    const int end = lo + n;
+    lo += k * step;
+    n = min(step, end - lo);
+  }
+  return lo;
 }
 
 __device__ __forceinline__ int find_request(const int32_t* cu, int B, int t) {
@@ -1010,8 +1048,13 @@ __device__ __forceinline__ int stop_from_state(unsigned long long st, int K) {
 }
 
 // Row metadata of target row t into shared memory (thread 0).
+// Run by warp 0.
 __device__ __noinline__ void row_meta(const Params& P, Smem& s, int t) {
-  const int b = find_request(P.cu, P.B, t);
+  const int lane = threadIdx.x & 31;
+  // The accept uniform is needed only after the row pass: load it now.
+  const float u = (lane == 0 && P.uniforms) ? __ldg(&P.uniforms[2 * (size_t)t]) : 0.f;
+  const int b = find_request_warp(P.cu, P.B, t, lane);
+  if (lane != 0) return;
   const int t0 = P.cu[b] + b, d0 = P.cu[b];
   const int K = P.cu[b + 1] - d0;
   const int i = t - t0;
@@ -1031,6 +1074,8 @@ __device__ __noinline__ void row_meta(const Params& P, Smem& s, int t) {
       xhat = -1;
     }
   }
+  s.u_acc = u;
+  s.zx_ok = 0;
   s.b = b;
   s.t0 = t0;
   s.d0 = d0;
@@ -1106,13 +1151,30 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
     ad.init();
     const bool has_d = drow != nullptr;
     if constexpr (VEC) {
+      // The thread whose vector holds the proposed token keeps its logits
+      // for the accept test, so that test needs no global load.
+      const int xh = s.xhat;
+      int kx = -1, vx = 0, jx = 0;
+      if (xh >= x0 && (size_t)(xh - x0) < len / Elem<DT>::kBytes) {
+        const int e = xh - x0;
+        kx = e / CH;
+        const int vi = (e - kx * CH) / EPV;
+        vx = vi / kThreads;
+        jx = (e - kx * CH) % EPV;
+        if (vi % kThreads != tid) kx = -1;
+      }
       ok = ring_stream(s, ring, trow + off, has_d ? drow + off : nullptr, len, false,
                        [&](int k, uint32_t stage) {
         uint4 rv[kVPT];
         stage_vectors<DT>(stage, x0 + k * CH, V, rv);
+        if (k == kx) {
+          s.zx_p = pick_element<DT>(rv, vx, jx);
+          s.zx_ok = 1;
+        }
         at.template add_raw<DT, kVPT>(rv, P.c);
         if (has_d) {
           stage_vectors<DT>(stage + kChunkBytes, x0 + k * CH, V, rv);
+          if (k == kx) s.zx_q = pick_element<DT>(rv, vx, jx);
           ad.template add_raw<DT, kVPT>(rv, P.c);
         }
       });
@@ -1200,20 +1262,20 @@ __device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const P
       if (xhat >= 0) {
         // p(x̂) = 2^(z c - mc_p) / S_p, and min(1, p/q) with q from the
         // draft row or q = 1 for a one-hot proposal.
-        const float zp = Elem<DT>::scalar(trow, xhat);
+        const float zp = s.zx_ok ? s.zx_p : Elem<DT>::scalar(trow, xhat);
         const float ap = fmaf(zp, P.c, -mcp);
         const double pd = (double)exp2f(ap) / Sp;
         double rho;
         double qd = 1.0;
         if (has_d) {
-          const float zq = Elem<DT>::scalar(drow, xhat);
+          const float zq = s.zx_ok ? s.zx_q : Elem<DT>::scalar(drow, xhat);
           const float aq = fmaf(zq, P.c, -mcq);
           qd = (double)exp2f(aq) / Sq;
           rho = (zq == -INFINITY) ? 0.0 : fmin(1.0, (double)exp2f(ap - aq) * (Sq / Sp));
         } else {
           rho = fmin(1.0, pd);
         }
-        const double u = (double)__ldg(&P.uniforms[2 * (size_t)t]);
+        const double u = (double)s.u_acc;
         acc = (u < rho) ? 1u : 0u;
         ph = (float)pd;
         qh = (float)qd;
@@ -1264,7 +1326,7 @@ template <int DT, bool VEC>
 __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int t, int part,
                              int split) {
   const int tid = threadIdx.x;
-  if (tid == 0) row_meta(P, s, t);
+  if (tid < 32) row_meta(P, s, t);
   __syncthreads();
   const int b = s.b, t0 = s.t0, d0 = s.d0, K = s.K, i = s.i;
   const bool greedy = s.greedy != 0;
