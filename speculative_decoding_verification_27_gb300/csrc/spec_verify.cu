@@ -370,12 +370,14 @@ __device__ __forceinline__ float pick_element(const uint4 (&rv)[kVPT], int v, in
 // ---------------------------------------------------------------------------
 // Streams `nbytes` of a row (and the same span of its paired row) through the
 // ring, first chunk first or (reverse) last chunk first; consume() gets the
-// chunk's index in the span. The k-th chunk streamed lands in stage
-// (seq + k) % kStages and completes on that
-// stage's full barrier; consume(k, stage_addr) is called by every thread once
-// the chunk has arrived, after which each warp releases the stage on its
+// chunk's index in the span and its shared-memory address. A stage holds a
+// chunk of each row, or, for a row streamed alone, two consecutive chunks of
+// it (one copy of twice the size, so a lone row keeps as many bytes in
+// flight as a pair). The k-th copy streamed lands in stage (seq + k) %
+// kStages and completes on that stage's full barrier; every thread consumes
+// the stage once it has arrived, after which each warp releases it on its
 // empty barrier. Thread 0 refills a stage only once all warps have released
-// its previous chunk, so warps never wait for each other inside the stream.
+// its previous copy, so warps never wait for each other inside the stream.
 // Every wait is bounded: a warp that gives up leaves the loop (warp-uniformly)
 // and the CTA then agrees on the failure; the copies still in flight are
 // waited for (bounded) and the ring must not be used again. Returns false on
@@ -385,29 +387,32 @@ __device__ __forceinline__ bool ring_stream(Smem& s, unsigned char* ring, const 
                                             const char* dptr, size_t nbytes, bool reverse,
                                             Consume&& consume) {
   const int tid = threadIdx.x, lane = tid & 31;
-  const int nch = (int)((nbytes + kChunkBytes - 1) / kChunkBytes);
+  const bool alone = dptr == nullptr;
+  const size_t copy_bytes = alone ? 2 * (size_t)kChunkBytes : (size_t)kChunkBytes;
+  const int nch = (int)((nbytes + copy_bytes - 1) / copy_bytes);
+  const int nlog = (int)((nbytes + kChunkBytes - 1) / kChunkBytes);  // chunks of the span
   const unsigned seq0 = s.ring_seq;
   const uint32_t ring_base = smem_addr(ring);
   const uint32_t full_base = smem_addr(&s.full[0]);
   const uint32_t empty_base = smem_addr(&s.empty[0]);
-  int issued = 0;    // chunks issued (thread 0)
+  int issued = 0;    // copies issued (thread 0)
   bool ok = true;    // thread 0's refill waits
   auto issue = [&](int k) {
     const unsigned q = seq0 + (unsigned)k;
     const int st = (int)(q % kStages);
-    // The stage's previous chunk (q - kStages) must have been released.
+    // The stage's previous copy (q - kStages) must have been released.
     if (q >= (unsigned)kStages && !mbar_wait(empty_base + 8u * st, ((q / kStages) - 1u) & 1u)) {
       ok = false;
       return;
     }
     const uint32_t bar = full_base + 8u * st;
-    const size_t off = (size_t)(reverse ? nch - 1 - k : k) * kChunkBytes;
+    const size_t off = (size_t)(reverse ? nch - 1 - k : k) * copy_bytes;
     const size_t left = nbytes - off;
-    const uint32_t bytes = (uint32_t)(left < (size_t)kChunkBytes ? left : (size_t)kChunkBytes);
+    const uint32_t bytes = (uint32_t)(left < copy_bytes ? left : copy_bytes);
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, dptr ? 2u * bytes : bytes);
+    mbar_arrive_expect_tx(bar, alone ? bytes : 2u * bytes);
     bulk_g2s(ring_base + (uint32_t)st * kStageBytes, tptr + off, bytes, bar);
-    if (dptr) bulk_g2s(ring_base + (uint32_t)st * kStageBytes + kChunkBytes, dptr + off, bytes, bar);
+    if (!alone) bulk_g2s(ring_base + (uint32_t)st * kStageBytes + kChunkBytes, dptr + off, bytes, bar);
     issued = k + 1;
   };
   if (tid == 0)
@@ -422,7 +427,14 @@ __device__ __forceinline__ bool ring_stream(Smem& s, unsigned char* ring, const 
       failed = true;
       break;
     }
-    consume(reverse ? nch - 1 - k : k, ring_base + (uint32_t)st * kStageBytes);
+    const int c = reverse ? nch - 1 - k : k;
+    const uint32_t stage = ring_base + (uint32_t)st * kStageBytes;
+    if (!alone) {
+      consume(c, stage);
+    } else {
+      consume(2 * c, stage);
+      if (2 * c + 1 < nlog) consume(2 * c + 1, stage + kChunkBytes);
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_base + 8u * st);
   }
