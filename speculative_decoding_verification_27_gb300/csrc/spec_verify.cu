@@ -113,7 +113,7 @@ constexpr int max_vocab(int dtype) { return kMaxScanTiles * kThreads * (dtype ==
 #define SV_MINBLOCKS 3
 #endif
 #ifndef SV_PART_CHUNKS
-#define SV_PART_CHUNKS 2
+#define SV_PART_CHUNKS 4
 #endif
 #ifndef SV_PUBLISH_WAVES
 #define SV_PUBLISH_WAVES 0
@@ -132,6 +132,7 @@ constexpr int kStageBytes = 2 * kChunkBytes;        // target + draft chunk
 constexpr int kRingBytes = kStages * kStageBytes;   // dynamic shared memory per CTA
 constexpr int kPartChunks = SV_PART_CHUNKS;         // ring chunks per draw part
 constexpr int kMaxParts = 16;                       // parts a draw is split into, at most
+constexpr size_t kMinPublishBytes = 192 * 1024;      // smallest draw worth splitting
 constexpr int kMaxDrawSlots = 4096;                 // draws that can be published per call
 // Draws are split into parts once at most kPublishWaves waves of rows are
 // left to hand out (0: once every row has been handed out).
@@ -950,12 +951,10 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
   if (tid == 0) __threadfence();
   for (int j = tid; j < stop; j += kThreads) P.out_tokens[t0 + j] = P.draft_tokens[d0 + j];
   const int srow = t0 + stop;
-  if (tid == 0) {
-    P.out_len[b] = stop + 1;
-    atomicAdd(&P.ws->committed, 1u);
-  }
+  if (tid == 0) P.out_len[b] = stop + 1;
   if (greedy) {
     if (tid == 0) {
+      atomicAdd(&P.ws->committed, 1u);
       P.out_tokens[srow] = __ldcg(&P.rows[srow].argmax);
       if (P.out_probs) {
         P.out_probs[2 * (size_t)(t0 + K)] = -1.f;
@@ -979,13 +978,22 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
   const float mcp = __ldcg(&P.rows[srow].mc_p), mcq = __ldcg(&P.rows[srow].mc_q);
   // Once the rows left fit in one wave, CTAs are about to fall idle: publish
   // the draw in parts so that they can share it, and take parts of it here.
+  // The request counts as committed only once its draw is published (or
+  // kept whole here), so that idle CTAs linger until they can take parts.
   if (tid == 0) {
     constexpr int TILE = kThreads * Elem<DT>::kEPV;
     const int nchunks = ((P.V + TILE - 1) / TILE + kVPT - 1) / kVPT;
-    int nparts = (nchunks + kPartChunks - 1) / kPartChunks;
+    // When every request's draw, cut into single chunks, fits in one wave of
+    // CTAs (a small batch), use single-chunk parts; otherwise larger ones.
+    int nparts = (long long)P.B * nchunks <= (long long)gridDim.x
+                     ? nchunks : (nchunks + kPartChunks - 1) / kPartChunks;
     nparts = nparts > kMaxParts ? kMaxParts : nparts;
+    // Parts carry a fixed cost (descriptor, ring start, a global merge); a
+    // draw that streams less than kMinPublishBytes is faster kept whole.
+    const size_t draw_bytes = (size_t)P.V * Elem<DT>::kBytes * (kind == kResidual ? 2 : 1);
     s.slot = -1;
-    if (nparts > 1 && ld_relaxed_gpu(&P.ws->next_item) + kPublishWaves * gridDim.x >= s.n_items) {
+    if (nparts > 1 && draw_bytes >= kMinPublishBytes &&
+        ld_relaxed_gpu(&P.ws->next_item) + kPublishWaves * gridDim.x >= s.n_items) {
       const unsigned slot = atomicAdd(&P.ws->n_draws, 1u);
       if (slot < (unsigned)P.n_slots) {
         DrawDesc* d = &P.descs[slot];
@@ -1005,6 +1013,7 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
         s.slot = (int)slot;
       }
     }
+    atomicAdd(&P.ws->committed, 1u);
   }
   __syncthreads();
   if (s.slot >= 0) {
@@ -1211,34 +1220,44 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
   return ok;
 }
 
-// Merges the statistics of a split row's parts (thread 0): the largest
-// exponent offset of the parts with mass and the sums rescaled to it in
-// fp64; for greedy rows the largest logit, lowest index among ties.
+// Merges the statistics of a split row's n <= 32 parts, one part per lane of
+// the calling warp; the result is valid in lane 0. The offset is the largest
+// exponent offset of the parts with mass, each part's sum is rescaled to it
+// by 2^(mc_r - mc) (the fp32 exponential the whole-row combine also uses) and
+// summed in fp64; greedy rows take the largest logit, lowest index on ties.
 __device__ __noinline__ PartRec merge_parts(const PartRec* parts, int n) {
+  const int lane = threadIdx.x & 31;
+  float mp = 0.f, mq = 0.f, av = -INFINITY;
+  double sp = 0.0, sq = 0.0;
+  int ai = 0x7fffffff;
+  if (lane < n) {
+    mp = __ldcg(&parts[lane].mc_p);
+    mq = __ldcg(&parts[lane].mc_q);
+    sp = __ldcg(&parts[lane].S_p);
+    sq = __ldcg(&parts[lane].S_q);
+    av = __ldcg(&parts[lane].amax_v);
+    ai = __ldcg(&parts[lane].amax_i);
+  }
+  const bool hp = sp > 0.0, hq = sq > 0.0;
+  const float Mp = warp_max(hp ? mp : -INFINITY), Mq = warp_max(hq ? mq : -INFINITY);
+  double wp = hp ? sp * (double)ex2(mp - Mp) : 0.0;
+  double wq = hq ? sq * (double)ex2(mq - Mq) : 0.0;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    wp += __shfl_xor_sync(kFull, wp, o);
+    wq += __shfl_xor_sync(kFull, wq, o);
+  }
+  warp_argmax(av, ai);
   PartRec m;
-  m.mc_p = m.mc_q = 0.f;
-  m.S_p = m.S_q = 0.0;
-  m.amax_v = -INFINITY;
-  m.amax_i = 0x7fffffff;
-  bool have_p = false, have_q = false;
-  for (int r = 0; r < n; ++r) {
-    const float mp = __ldcg(&parts[r].mc_p), mq = __ldcg(&parts[r].mc_q);
-    if (__ldcg(&parts[r].S_p) > 0.0 && (!have_p || mp > m.mc_p)) { m.mc_p = mp; have_p = true; }
-    if (__ldcg(&parts[r].S_q) > 0.0 && (!have_q || mq > m.mc_q)) { m.mc_q = mq; have_q = true; }
-    float v = __ldcg(&parts[r].amax_v);
-    int ix = __ldcg(&parts[r].amax_i);
-    argmax_merge(m.amax_v, m.amax_i, v, ix);
-  }
-  for (int r = 0; r < n; ++r) {
-    const double sp = __ldcg(&parts[r].S_p), sq = __ldcg(&parts[r].S_q);
-    if (sp > 0.0) m.S_p += sp * exp2((double)__ldcg(&parts[r].mc_p) - (double)m.mc_p);
-    if (sq > 0.0) m.S_q += sq * exp2((double)__ldcg(&parts[r].mc_q) - (double)m.mc_q);
-  }
+  m.mc_p = Mp == -INFINITY ? 0.f : Mp;
+  m.mc_q = Mq == -INFINITY ? 0.f : Mq;
+  m.S_p = wp;
+  m.S_q = wq;
+  m.amax_v = av;
+  m.amax_i = ai;
   return m;
 }
 
-// Decision for row t from its statistics (thread 0): the row record, the
-// slot's (p(x̂), q(x̂)), and whether this row completes its request.
 template <int DT>
 __device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const PartRec& st) {
   const int b = s.b, d0 = s.d0, K = s.K, i = s.i, xhat = s.xhat;
@@ -1364,12 +1383,15 @@ __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int 
       s.merge = (old == (unsigned)np - 1u) ? 1 : 0;  // this CTA merges the row
       if (s.merge) {
         __threadfence();
-        st = merge_parts(P.parts + (size_t)split * np, np);
         P.part_done[split] = 0u;
       }
     }
     __syncthreads();
     if (!s.merge) return true;
+    if (tid < 32) {
+      const PartRec m = merge_parts(P.parts + (size_t)split * np, np);
+      if (tid == 0) st = m;
+    }
   }
   if (tid == 0) decide_row<DT>(P, s, t, st);
   __syncthreads();
