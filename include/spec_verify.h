@@ -89,10 +89,11 @@ enum { SV_MODE_SAMPLE = 0, SV_MODE_GREEDY = 1 };
  * Bytes of workspace spec_verify / spec_verify_greedy need for B requests,
  * R_t target rows and vocabulary size V (0 if an argument is out of range).
  * The workspace holds a 64-byte header, an 8-byte progress word per request, a 32-byte
- * record per target row, a fixed 528 KiB region for rows that the kernel
- * splits across CTAs near the end of a call, and, for up to min(B, 4096)
- * final draws it splits the same way, a descriptor and the partial sums of
- * each. It must be 16-byte aligned and zero-filled
+ * record per target row, the tile sums (8 bytes per 1024 vocabulary entries)
+ * that each request's bonus row leaves for its draw, a fixed 528 KiB region
+ * for rows that the kernel splits across CTAs near the end of a call, and,
+ * for up to min(B, 4096) final draws it splits the same way, a descriptor and
+ * the partial sums of each. It must be 16-byte aligned and zero-filled
  * before its first use; every call leaves its counters at zero again, so
  * calls in stream order may reuse it without clearing. Calls that may run
  * concurrently (other streams) need distinct workspaces.

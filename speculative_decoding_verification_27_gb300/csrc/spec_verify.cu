@@ -61,7 +61,8 @@ struct alignas(16) RowRec {
   double S_p;        // sum_x 2^(z_x c - mc_p) over the target row
   double S_q;        // same over the draft row
   int argmax;        // greedy rows: first index of the maximum
-  unsigned accept;   // 1 if the slot's draft token is accepted
+  unsigned accept;   // bit 0: the slot's draft token is accepted; bit 1 (bonus
+                     // rows): the tile sums of r = 2^(z c - mc_p) are stored
 };
 static_assert(sizeof(RowRec) == 32, "row record is 32 bytes");
 
@@ -172,6 +173,7 @@ struct Params {
   unsigned int* slot_state; // [n_slots] nparts << 20 | parts handed out (0: unpublished)
   DrawDesc* descs;          // [n_slots]
   double* tsum;             // [n_slots, tsum_stride] per-tile sums of r
+  double* btile;            // [B, tsum_stride] tile sums of a bonus row's r = S_p p
   int n_slots, tsum_stride;
   unsigned int* part_done;  // [kMaxTailRows] parts finished per split row
   PartRec* parts;           // [kMaxPartRecs]
@@ -188,6 +190,7 @@ struct Smem {
   unsigned n_items, r_full, row_parts;  // work-item layout of this launch
   int b, t0, d0, K, i, greedy, xhat, last, stop, merge, pick, pick2, tok;
   int zx_ok;        // z_p(x̂) (and z_q(x̂)) were taken from the ring during the row pass
+  int btile_ok;     // this bonus row's tile sums were stored during its pass
   float zx_p, zx_q, u_acc;
   float redf[kWarps];
   float redf2[kWarps];
@@ -306,6 +309,27 @@ struct SoftAcc {
     for (int i = 0; i < kPairs; ++i) z[i] = f2_pack(f[2 * i], f[2 * i + 1]);
     accumulate(z, f2_splat(c), f2_splat(-mc));
   }
+  // As add_raw, also returning each vector's own sum of terms (relative to
+  // this thread's offset mc after the chunk); the running sums are the same.
+  template <int DT, int N>
+  __device__ __forceinline__ void add_raw_tiles(const uint4 (&v)[N], float c, float (&tv)[N]) {
+    raise(Raw<DT>::template max_of<N>(v), c);
+    const f2_t cc = f2_splat(c), nmc = f2_splat(-mc);
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+      f2_t z[kPairs], acc = 0ull;
+      Raw<DT>::pairs(v[u], z);
+#pragma unroll
+      for (int i = 0; i < kPairs; ++i) {
+        const f2_t e = f2_ex2(f2_fma(z[i], cc, nmc));
+        a[i] = f2_add(a[i], e);
+        acc = f2_add(acc, e);
+      }
+      float lo, hi;
+      f2_unpack(acc, lo, hi);
+      tv[u] = lo + hi;
+    }
+  }
   // N raw vectors at once: one maximum and one rescale check.
   template <int DT, int N>
   __device__ __forceinline__ void add_raw(const uint4 (&v)[N], float c) {
@@ -346,6 +370,28 @@ __device__ __forceinline__ void stage_vectors(uint32_t stage, int x, int V, uint
       rv[v] = (x + vi * EPV < V) ? lds16(stage + 16u * vi) : make_uint4(n, n, n, n);
     }
   }
+}
+
+// Warp totals of kVPT per-lane values (one per tile of a chunk): each
+// halving step trades half of the tiles with the partner lane, then a plain
+// butterfly. Returns the total of tile `t`, valid in lanes whose low
+// log2(32 / kVPT) bits are zero (lane j * (32 / kVPT) holds tile j).
+__device__ __forceinline__ float warp_tile_totals(float (&ts)[kVPT], int lane, int& t) {
+  t = 0;
+#pragma unroll
+  for (int half = kVPT / 2, o = 16; half >= 1; half /= 2, o /= 2) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? ts[i] : ts[i + half];
+      const float keep = up ? ts[i + half] : ts[i];
+      ts[i] = keep + __shfl_xor_sync(kFull, send, o);
+    }
+    if (up) t += half;
+  }
+#pragma unroll
+  for (int o = 16 / kVPT; o >= 1; o /= 2) ts[0] += __shfl_xor_sync(kFull, ts[0], o);
+  return ts[0];
 }
 
 // Element j of vector v of rv (run once per row, by one thread).
@@ -700,25 +746,10 @@ __device__ bool tile_sums(const Params& P, Smem& s, unsigned char* ring, const D
         f2_unpack(acc, lo, hi);
         ts[v] = lo + hi;
       }
-      // Warp totals of the chunk's kVPT tiles: each halving step trades half
-      // of the tiles with the partner lane, then a plain butterfly; lane
-      // j * (32 / kVPT) ends with the total of tile j.
-      int t = 0;
-#pragma unroll
-      for (int half = kVPT / 2, o = 16; half >= 1; half /= 2, o /= 2) {
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-          const float send = up ? ts[i] : ts[i + half];
-          const float keep = up ? ts[i + half] : ts[i];
-          ts[i] = keep + __shfl_xor_sync(kFull, send, o);
-        }
-        if (up) t += half;
-      }
-#pragma unroll
-      for (int o = 16 / kVPT; o >= 1; o /= 2) ts[0] += __shfl_xor_sync(kFull, ts[0], o);
+      int t;
+      const float tot = warp_tile_totals(ts, lane, t);
       const int l = k * kVPT + t;
-      if ((lane & (32 / kVPT - 1)) == 0 && l < ntl) s.wtot[l * kWarps + warp] = ts[0];
+      if ((lane & (32 / kVPT - 1)) == 0 && l < ntl) s.wtot[l * kWarps + warp] = tot;
     });
   } else {
     for (int l = 0; l < ntl; ++l) {
@@ -976,6 +1007,22 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
   }
   const double Sp = __ldcg(&P.rows[srow].S_p), Sq = __ldcg(&P.rows[srow].S_q);
   const float mcp = __ldcg(&P.rows[srow].mc_p), mcq = __ldcg(&P.rows[srow].mc_q);
+  if (VEC && kind == kBonus && (__ldcg(&P.rows[srow].accept) & 2u)) {
+    // The bonus row left its tile sums: only the chosen tile is read again.
+    if (tid == 0) atomicAdd(&P.ws->committed, 1u);
+    const DrawArgs a = make_draw_args(P, (size_t)P.V * Elem<DT>::kBytes, srow, drow, kind, xhat,
+                                      mcp, mcq, Sp, Sq);
+    constexpr int TILE = kThreads * Elem<DT>::kEPV;
+    const int ntiles = (P.V + TILE - 1) / TILE;
+    const double tt = tid < ntiles ? __ldcg(&P.btile[(size_t)b * P.tsum_stride + tid]) : 0.0;
+    int y = locate_token<DT, VEC>(P, s, a, tt, ntiles);
+    if (y < 0) {
+      if (tid == 0) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
+      y = 0;
+    }
+    if (tid == 0) finish_draw<DT>(P, a, Sp, Sq, y, t0 + K);
+    return true;
+  }
   // Once the rows left fit in one wave, CTAs are about to fall idle: publish
   // the draw in parts so that they can share it, and take parts of it here.
   // The request counts as committed only once its draw is published (or
@@ -1097,6 +1144,7 @@ __device__ __noinline__ void row_meta(const Params& P, Smem& s, int t) {
   }
   s.u_acc = u;
   s.zx_ok = 0;
+  s.btile_ok = 0;
   s.b = b;
   s.t0 = t0;
   s.d0 = d0;
@@ -1111,7 +1159,8 @@ __device__ __noinline__ void row_meta(const Params& P, Smem& s, int t) {
 // the CTA into `st` (valid in thread 0). Returns false on a copy timeout.
 template <int DT, bool VEC>
 __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const char* trow,
-                            const char* drow, bool greedy, int c0, int c1, PartRec& st) {
+                            const char* drow, bool greedy, int c0, int c1, PartRec& st,
+                            bool btiles, int b) {
   constexpr int EPV = Elem<DT>::kEPV;
   constexpr int CH = kChunkBytes / Elem<DT>::kBytes;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1184,21 +1233,47 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
         jx = (e - kx * CH) % EPV;
         if (vi % kThreads != tid) kx = -1;
       }
-      ok = ring_stream(s, ring, trow + off, has_d ? drow + off : nullptr, len, false,
-                       [&](int k, uint32_t stage) {
-        uint4 rv[kVPT];
-        stage_vectors<DT>(stage, x0 + k * CH, V, rv);
-        if (k == kx) {
-          s.zx_p = pick_element<DT>(rv, vx, jx);
-          s.zx_ok = 1;
-        }
-        at.template add_raw<DT, kVPT>(rv, P.c);
-        if (has_d) {
-          stage_vectors<DT>(stage + kChunkBytes, x0 + k * CH, V, rv);
-          if (k == kx) s.zx_q = pick_element<DT>(rv, vx, jx);
-          ad.template add_raw<DT, kVPT>(rv, P.c);
-        }
-      });
+      // A bonus row (whole, r = S_p p if it is drawn from) also leaves, per
+      // tile and warp, the sum of its terms relative to a per-chunk warp
+      // offset, in the draw's scratch (idle during a row pass).
+      float* bref = reinterpret_cast<float*>(s.tincl);  // [chunk][warp] offsets
+      constexpr int TILE = kThreads * EPV;
+      const int ntiles = (V + TILE - 1) / TILE;
+      if (btiles) {
+        // Bonus rows stream alone (no draft row, no proposed token).
+        ok = ring_stream(s, ring, trow + off, nullptr, len, false, [&](int k, uint32_t stage) {
+          uint4 rv[kVPT];
+          stage_vectors<DT>(stage, x0 + k * CH, V, rv);
+          float tv[kVPT];
+          at.template add_raw_tiles<DT, kVPT>(rv, P.c, tv);
+          const bool live = at.m != -INFINITY;
+          const float ref = warp_max(live ? at.mc : -INFINITY);
+          const float f = live ? ex2(at.mc - ref) : 0.f;
+#pragma unroll
+          for (int v = 0; v < kVPT; ++v) tv[v] *= f;
+          int t;
+          const float tot = warp_tile_totals(tv, lane, t);
+          const int l = k * kVPT + t;
+          if ((lane & (32 / kVPT - 1)) == 0 && l < ntiles) s.wtot[l * kWarps + warp] = tot;
+          if (lane == 0) bref[k * kWarps + warp] = ref;
+        });
+      } else {
+        ok = ring_stream(s, ring, trow + off, has_d ? drow + off : nullptr, len, false,
+                         [&](int k, uint32_t stage) {
+          uint4 rv[kVPT];
+          stage_vectors<DT>(stage, x0 + k * CH, V, rv);
+          if (k == kx) {
+            s.zx_p = pick_element<DT>(rv, vx, jx);
+            s.zx_ok = 1;
+          }
+          at.template add_raw<DT, kVPT>(rv, P.c);
+          if (has_d) {
+            stage_vectors<DT>(stage + kChunkBytes, x0 + k * CH, V, rv);
+            if (k == kx) s.zx_q = pick_element<DT>(rv, vx, jx);
+            ad.template add_raw<DT, kVPT>(rv, P.c);
+          }
+        });
+      }
     } else {
       if (has_d)
         stats_pass_scalar<DT, true>(trow, drow, V, P.c, at, ad);
@@ -1208,6 +1283,26 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
     float mcp, mcq;
     double Sp, Sq;
     combine_softmax<EPV>(at, ad, has_d, P.c, s, mcp, Sp, mcq, Sq);
+    if (VEC && btiles && ok) {
+      // Tile sums of r = 2^(z c - mc_p): each warp's part rescaled from its
+      // chunk offset to the row's, summed over the warps in fp64.
+      if (tid == 0) s.bcast_f[0] = mcp;
+      __syncthreads();
+      const float M = s.bcast_f[0];
+      constexpr int TILE = kThreads * EPV;
+      const int ntiles = (V + TILE - 1) / TILE;
+      const float* bref = reinterpret_cast<const float*>(s.tincl);
+      if (tid < ntiles) {
+        const int k = tid / kVPT;
+        double T = 0.0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+          T += (double)(s.wtot[tid * kWarps + w] * ex2(bref[k * kWarps + w] - M));
+        P.btile[(size_t)b * P.tsum_stride + tid] = T;
+      }
+      if (tid == 0) s.btile_ok = 1;
+      __syncthreads();
+    }
     if (tid == 0) {
       st.mc_p = mcp;
       st.mc_q = mcq;
@@ -1285,7 +1380,7 @@ __device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const P
     rec.S_p = Sp;
     rec.S_q = Sq;
     rec.argmax = 0;
-    rec.accept = 1u;
+    rec.accept = (i == K && s.btile_ok) ? 3u : 1u;
     if (!(Sp > 0.0) || (has_d && !(Sq > 0.0))) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
     if (i < K) {
       float ph = -1.f, qh = -1.f;
@@ -1374,7 +1469,8 @@ __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int 
     c1 = min(nch, c0 + cpp);
   }
   PartRec st;
-  if (!slice_stats<DT, VEC>(P, s, ring, trow, drow, greedy, c0, c1, st)) return false;
+  const bool btiles = VEC && part < 0 && i == K && !greedy;
+  if (!slice_stats<DT, VEC>(P, s, ring, trow, drow, greedy, c0, c1, st, btiles, b)) return false;
   if (part >= 0) {
     if (tid == 0) {
       P.parts[(size_t)split * np + part] = st;
@@ -1527,9 +1623,9 @@ static int n_draw_slots(long long B) { return (int)(B < kMaxDrawSlots ? B : kMax
 static int tsum_stride(int V) { return (V + kThreads * 4 - 1) / (kThreads * 4); }
 
 // header | req_state[B] | slot_state[S] | descs[S] | tsum[S][stride] |
-// part_done[kMaxTailRows] | parts[kMaxPartRecs] | rows[R_t]
+// btile[B][stride] | part_done[kMaxTailRows] | parts[kMaxPartRecs] | rows[R_t]
 struct WsLayout {
-  size_t req_done, slot_state, descs, tsum, part_done, parts, rows;
+  size_t req_done, slot_state, descs, tsum, btile, part_done, parts, rows;
 };
 
 static WsLayout ws_layout(long long B, int V) {
@@ -1539,7 +1635,8 @@ static WsLayout ws_layout(long long B, int V) {
   L.slot_state = L.req_done + align16((size_t)B * sizeof(unsigned long long));
   L.descs = L.slot_state + align16(S * sizeof(unsigned));
   L.tsum = L.descs + S * sizeof(DrawDesc);
-  L.part_done = L.tsum + align16(S * (size_t)tsum_stride(V) * sizeof(double));
+  L.btile = L.tsum + align16(S * (size_t)tsum_stride(V) * sizeof(double));
+  L.part_done = L.btile + align16((size_t)B * tsum_stride(V) * sizeof(double));
   L.parts = L.part_done + align16((size_t)kMaxTailRows * sizeof(unsigned));
   L.rows = L.parts + (size_t)kMaxPartRecs * sizeof(PartRec);
   return L;
@@ -1636,6 +1733,7 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
   P.slot_state = reinterpret_cast<unsigned*>(ws + L.slot_state);
   P.descs = reinterpret_cast<DrawDesc*>(ws + L.descs);
   P.tsum = reinterpret_cast<double*>(ws + L.tsum);
+  P.btile = reinterpret_cast<double*>(ws + L.btile);
   P.n_slots = n_draw_slots(B);
   P.part_done = reinterpret_cast<unsigned*>(ws + L.part_done);
   P.parts = reinterpret_cast<PartRec*>(ws + L.parts);
