@@ -116,8 +116,8 @@ constexpr int max_vocab(int dtype) { return kMaxScanTiles * kThreads * (dtype ==
 #ifndef SV_PART_CHUNKS
 #define SV_PART_CHUNKS 4
 #endif
-#ifndef SV_PUBLISH_WAVES
-#define SV_PUBLISH_WAVES 0
+#ifndef SV_PUBLISH_PCT
+#define SV_PUBLISH_PCT 0
 #endif
 #ifndef SV_ROW_PARTS
 #define SV_ROW_PARTS 1
@@ -135,9 +135,9 @@ constexpr int kPartChunks = SV_PART_CHUNKS;         // ring chunks per draw part
 constexpr int kMaxParts = 16;                       // parts a draw is split into, at most
 constexpr size_t kMinPublishBytes = 192 * 1024;      // smallest draw worth splitting
 constexpr int kMaxDrawSlots = 4096;                 // draws that can be published per call
-// Draws are split into parts once at most kPublishWaves waves of rows are
-// left to hand out (0: once every row has been handed out).
-constexpr unsigned kPublishWaves = SV_PUBLISH_WAVES;
+// Draws are split into parts once the rows still to be handed out number at
+// most kPublishPct percent of the grid (0: once all rows are handed out).
+constexpr unsigned kPublishPct = SV_PUBLISH_PCT;
 // Rows may be split into parts that different CTAs stream; the CTA that
 // finishes a row's last part merges the parts' statistics. Every row is
 // split when there are fewer rows than CTAs (small batches); the last
@@ -1040,7 +1040,7 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
     const size_t draw_bytes = (size_t)P.V * Elem<DT>::kBytes * (kind == kResidual ? 2 : 1);
     s.slot = -1;
     if (nparts > 1 && draw_bytes >= kMinPublishBytes &&
-        ld_relaxed_gpu(&P.ws->next_item) + kPublishWaves * gridDim.x >= s.n_items) {
+        ld_relaxed_gpu(&P.ws->next_item) + kPublishPct * gridDim.x / 100u >= s.n_items) {
       const unsigned slot = atomicAdd(&P.ws->n_draws, 1u);
       if (slot < (unsigned)P.n_slots) {
         DrawDesc* d = &P.descs[slot];
