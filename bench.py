@@ -41,8 +41,8 @@ WORKLOAD = ("sampling verify B=256 K=7 V=151936 bf16 T=0.7, peaked rank-score ro
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per verify launch on this workload from one ncu
 # capture, valid only for the kernel sources whose hash is recorded with it.
-TRAFFIC = {"sources_sha256": "411d282be53444e2c5c1713a2ae1a0b653a233d33cdf9950a79f0443e8d42136",
-           "bytes_per_launch": 1273348000 + 4961024,
+TRAFFIC = {"sources_sha256": "dd29b8c0bdf0ebe8b9e2f1d999e8897d20214c3af930349a18066ea027d51c96",
+           "bytes_per_launch": 1233614000 + 5711872,
            "profile": "profiles/verify_kernel_sampling_B256_K7_V151936_bf16.md"}
 
 
