@@ -7,10 +7,9 @@
 // token after it; propose what followed, cut to max_tokens.
 //
 // One CTA per history. The history is staged in shared memory when it fits;
-// for each n the CTA tests 256 candidate starts at a time, from the most
-// recent down, and stops at the first window holding a match (the largest
-// matching start of that window wins). All comparisons are on integers, so
-// the result is bit-exact.
+// for each n every thread tests its own candidate starts from the most recent
+// down and stops at its first match; the largest over the threads wins. All
+// comparisons are on integers, so the result is bit-exact.
 #include "../../include/spec_verify.h"
 
 #include <cstdint>
@@ -25,8 +24,8 @@ __global__ void __launch_bounds__(kNgThreads) ngram_kernel(
     const int32_t* __restrict__ hist, long long stride, const int32_t* __restrict__ hist_len,
     int min_n, int max_n, int max_tokens, int32_t* __restrict__ out_tokens,
     int32_t* __restrict__ out_count, int32_t* __restrict__ out_n, int staged) {
-  extern __shared__ int32_t sh_hist[];
-  __shared__ int s_best;
+  extern __shared__ __align__(16) int32_t sh_hist[];
+  __shared__ int s_warp_best[kNgThreads / 32];
   const int b = blockIdx.x, tid = threadIdx.x;
   const int32_t* g = hist + (long long)b * stride;
   int L = hist_len[b];
@@ -34,7 +33,17 @@ __global__ void __launch_bounds__(kNgThreads) ngram_kernel(
   if ((long long)L > stride) L = (int)stride;
   const int32_t* h = g;
   if (staged) {
-    for (int k = tid; k < L; k += kNgThreads) sh_hist[k] = g[k];
+    // 16-byte loads when the row allows them, several in flight per thread.
+    int done = 0;
+    if ((reinterpret_cast<uintptr_t>(g) & 15) == 0) {
+      const int nv = L >> 2;
+      const int4* gv = reinterpret_cast<const int4*>(g);
+      int4* sv = reinterpret_cast<int4*>(sh_hist);
+#pragma unroll 4
+      for (int k = tid; k < nv; k += kNgThreads) sv[k] = __ldg(gv + k);
+      done = nv << 2;
+    }
+    for (int k = done + tid; k < L; k += kNgThreads) sh_hist[k] = g[k];
     __syncthreads();
     h = sh_hist;
   }
@@ -43,30 +52,32 @@ __global__ void __launch_bounds__(kNgThreads) ngram_kernel(
   for (int n = nhi; n >= min_n && found_n == 0; --n) {
     const int tail = L - n;
     // Largest start whose match ends before the tail and leaves a token.
-    const int hi = tail - n - 1;
-    for (int base = hi; base >= 0; base -= kNgThreads) {
-      const int s = base - tid;
-      bool match = false;
-      if (s >= 0) {
-        match = true;
-        for (int j = 0; j < n; ++j) {
-          if (h[s + j] != h[tail + j]) {
-            match = false;
-            break;
-          }
+    // Each thread walks its own candidates downwards, so its first match is
+    // its largest; the CTA then takes the largest over the threads.
+    int best = -1;
+    for (int st = tail - n - 1 - tid; st >= 0; st -= kNgThreads) {
+      bool match = true;
+      for (int j = 0; j < n; ++j) {
+        if (h[st + j] != h[tail + j]) {
+          match = false;
+          break;
         }
       }
-      if (tid == 0) s_best = -1;
-      __syncthreads();
-      if (match) atomicMax(&s_best, s);
-      __syncthreads();
-      const int best = s_best;
-      __syncthreads();
-      if (best >= 0) {
-        found_n = n;
-        found_s = best;
+      if (match) {
+        best = st;
         break;
       }
+    }
+    best = __reduce_max_sync(0xffffffffu, best);
+    if ((tid & 31) == 0) s_warp_best[tid >> 5] = best;
+    __syncthreads();
+    best = s_warp_best[0];
+#pragma unroll
+    for (int w = 1; w < kNgThreads / 32; ++w) best = max(best, s_warp_best[w]);
+    __syncthreads();  // s_warp_best is reused by the next window length
+    if (best >= 0) {
+      found_n = n;
+      found_s = best;
     }
   }
   int cnt = 0;

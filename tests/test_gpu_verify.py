@@ -216,3 +216,47 @@ def test_chi_square_through_the_gpu(cuda_lib):
     alpha = np.minimum(p, q).sum()
     acc = (ln.cpu().numpy() == 2).mean()
     assert abs(acc - alpha) < 5 * np.sqrt(alpha * (1 - alpha) / N)
+
+
+# --------------------------------------------------------------------------
+# n-gram proposer edge cases
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("min_n,max_n,max_tokens", [(1, 1, 4), (1, 3, 5), (2, 4, 1), (3, 3, 0), (2, 6, 9)])
+def test_ngram_small_random_histories_bit_exact(cuda_lib, min_n, max_n, max_tokens):
+    """Tiny vocabulary (many matches), lengths 0..64 in rows of stride 80."""
+    import oracle
+    rng = np.random.default_rng(1000 + 10 * min_n + max_n)
+    B, stride = 300, 80
+    hist = rng.integers(0, 4, size=(B, stride)).astype(np.int32)
+    hl = rng.integers(0, 65, size=B).astype(np.int32)
+    hl[:4] = [0, 1, 2, 64]
+    out, cnt, nn = api.ngram_propose(torch.from_numpy(hist).cuda(), torch.from_numpy(hl).cuda(),
+                                     min_n, max_n, max_tokens)
+    torch.cuda.synchronize()
+    o_out, o_cnt, o_n = oracle.ngram_propose(hist, hl, min_n, max_n, max_tokens)
+    assert np.array_equal(cnt.cpu().numpy(), o_cnt)
+    assert np.array_equal(nn.cpu().numpy(), o_n)
+    g = out.cpu().numpy()
+    for b in range(B):
+        assert np.array_equal(g[b, :o_cnt[b]], o_out[b, :o_cnt[b]])
+        assert np.all(g[b, o_cnt[b]:] == -1)
+
+
+def test_ngram_long_history_read_from_global(cuda_lib):
+    """Histories longer than the shared-memory staging limit (12288 tokens)."""
+    import oracle
+    rng = np.random.default_rng(77)
+    B, L = 6, 20000
+    hist = rng.integers(0, 32000, size=(B, L)).astype(np.int32)
+    hist[0, 100:140] = hist[0, L - 40:L]      # early copy of the tail
+    hist[1, 15000:15010] = hist[1, L - 10:L]  # late copy
+    hl = np.full(B, L, np.int32)
+    hl[5] = 3
+    out, cnt, nn = api.ngram_propose(torch.from_numpy(hist).cuda(), torch.from_numpy(hl).cuda(), 2, 4, 6)
+    torch.cuda.synchronize()
+    o_out, o_cnt, o_n = oracle.ngram_propose(hist, hl, 2, 4, 6)
+    assert np.array_equal(cnt.cpu().numpy(), o_cnt) and np.array_equal(nn.cpu().numpy(), o_n)
+    assert o_cnt[0] > 0 and o_cnt[1] > 0
+    g = out.cpu().numpy()
+    for b in range(B):
+        assert np.array_equal(g[b, :o_cnt[b]], o_out[b, :o_cnt[b]])
