@@ -41,18 +41,21 @@ WORKLOAD = ("sampling verify B=256 K=7 V=151936 bf16 T=0.7, peaked rank-score ro
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per verify launch on this workload from one ncu
 # capture, valid only for the kernel sources whose hash is recorded with it.
-TRAFFIC = {"sources_sha256": "dd29b8c0bdf0ebe8b9e2f1d999e8897d20214c3af930349a18066ea027d51c96",
+TRAFFIC = {"sources_sha256": "0d5792ca242477a800d78d3a955fd4708477a0977993fb0bea6e9fd89ff60465",
            "bytes_per_launch": 1233614000 + 5711872,
            "profile": "profiles/verify_kernel_sampling_B256_K7_V151936_bf16.md"}
 
 
-def kernel_sources_hash() -> str:
+VERIFY_SOURCES = ("spec_verify.cu", "sv_device.cuh")
+
+
+def kernel_sources_hash(names=VERIFY_SOURCES) -> str:
+    """sha256 over the named kernel sources (the verify kernel's by default)."""
     d = os.path.join(ROOT, "speculative_decoding_verification_27_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(f.encode())
-            h.update(open(os.path.join(d, f), "rb").read())
+    for f in sorted(names):
+        h.update(f.encode())
+        h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()
 
 
