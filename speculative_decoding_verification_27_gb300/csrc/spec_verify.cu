@@ -444,6 +444,11 @@ __device__ __forceinline__ bool ring_stream(Smem& s, unsigned char* ring, const 
   const uint32_t empty_base = smem_addr(&s.empty[0]);
   int issued = 0;    // copies issued (thread 0)
   bool ok = true;    // thread 0's refill waits
+  // L2 priority: a row pass reads its bytes once, so they go first and the
+  // small data every CTA keeps touching (offsets, tokens, uniforms, row
+  // records) stays in L2; a draw's bytes stay, because the draw rescans the
+  // chosen tile right after its pass.
+  const uint64_t pol = (tid == 0) ? (reverse ? l2_policy_evict_last() : l2_policy_evict_first()) : 0ull;
   auto issue = [&](int k) {
     const unsigned q = seq0 + (unsigned)k;
     const int st = (int)(q % kStages);
@@ -458,8 +463,9 @@ __device__ __forceinline__ bool ring_stream(Smem& s, unsigned char* ring, const 
     const uint32_t bytes = (uint32_t)(left < copy_bytes ? left : copy_bytes);
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(bar, alone ? bytes : 2u * bytes);
-    bulk_g2s(ring_base + (uint32_t)st * kStageBytes, tptr + off, bytes, bar);
-    if (!alone) bulk_g2s(ring_base + (uint32_t)st * kStageBytes + kChunkBytes, dptr + off, bytes, bar);
+    bulk_g2s_hint(ring_base + (uint32_t)st * kStageBytes, tptr + off, bytes, bar, pol);
+    if (!alone)
+      bulk_g2s_hint(ring_base + (uint32_t)st * kStageBytes + kChunkBytes, dptr + off, bytes, bar, pol);
     issued = k + 1;
   };
   if (tid == 0)
