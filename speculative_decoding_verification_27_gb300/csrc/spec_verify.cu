@@ -151,7 +151,16 @@ constexpr unsigned kMaxPartRecs = 16384;            // part records, at most
 // A CTA with no rows left looks for draw parts until every request has
 // committed, sleeping kLingerNs between looks, at most kLingerPolls times.
 // Giving up early is harmless: a draw's owner takes its remaining parts.
-constexpr unsigned kLingerNs = 500;
+#ifndef SV_BONUS_LAST
+#define SV_BONUS_LAST 1
+#endif
+#ifndef SV_LINGER_NS
+#define SV_LINGER_NS 500
+#endif
+constexpr unsigned kLingerNs = SV_LINGER_NS;
+// Work order: rows in target-row order, or (kBonusLast) every draft-slot row
+// first and the requests' bonus rows last.
+constexpr bool kBonusLast = SV_BONUS_LAST != 0;
 constexpr unsigned kLingerPolls = 1u << 16;
 
 enum DrawKind { kResidual = 0, kOneHot = 1, kBonus = 2 };
@@ -188,7 +197,7 @@ struct Smem {
   unsigned ring_seq;                  // chunks this CTA has streamed so far
   int wk, item, slot, part;
   unsigned n_items, r_full, row_parts;  // work-item layout of this launch
-  int b, t0, d0, K, i, greedy, xhat, last, stop, merge, pick, pick2, tok;
+  int b, t, t0, d0, K, i, greedy, xhat, last, stop, merge, pick, pick2, tok, R_d;
   int zx_ok;        // z_p(x̂) (and z_q(x̂)) were taken from the ring during the row pass
   int btile_ok;     // this bonus row's tile sums were stored during its pass
   float zx_p, zx_q, u_acc;
@@ -1122,12 +1131,39 @@ __device__ __forceinline__ int stop_from_state(unsigned long long st, int K) {
 }
 
 // Row metadata of target row t into shared memory (thread 0).
-// Run by warp 0.
-__device__ __noinline__ void row_meta(const Params& P, Smem& s, int t) {
+// Largest b in [0, B) with cu[b] <= j (the request owning draft slot j), by
+// a whole warp as find_request_warp.
+__device__ __forceinline__ int find_draft_request_warp(const int32_t* cu, int B, int j, int lane) {
+  int lo = 0, n = B;
+  while (n > 1) {
+    const int step = (n + 31) >> 5;
+    const int c = lo + lane * step;
+    const bool pass = c < lo + n && cu[c] <= j;
+    const unsigned m = __ballot_sync(kFull, pass);
+    const int k = 31 - __clz(m);
+    const int end = lo + n;
+    lo += k * step;
+    n = min(step, end - lo);
+  }
+  return lo;
+}
+
+// Run by warp 0: the row at position o of the work order.
+__device__ __noinline__ void row_meta(const Params& P, Smem& s, int o) {
   const int lane = threadIdx.x & 31;
+  int b, t;
+  if (!kBonusLast) {
+    t = o;
+    b = find_request_warp(P.cu, P.B, t, lane);
+  } else if (o < s.R_d) {  // draft-slot rows first, in order
+    b = find_draft_request_warp(P.cu, P.B, o, lane);
+    t = o + b;
+  } else {                 // then the bonus rows
+    b = o - s.R_d;
+    t = P.cu[b + 1] + b;
+  }
   // The accept uniform is needed only after the row pass: load it now.
   const float u = (lane == 0 && P.uniforms) ? __ldg(&P.uniforms[2 * (size_t)t]) : 0.f;
-  const int b = find_request_warp(P.cu, P.B, t, lane);
   if (lane != 0) return;
   const int t0 = P.cu[b] + b, d0 = P.cu[b];
   const int K = P.cu[b + 1] - d0;
@@ -1152,6 +1188,7 @@ __device__ __noinline__ void row_meta(const Params& P, Smem& s, int t) {
   s.zx_ok = 0;
   s.btile_ok = 0;
   s.b = b;
+  s.t = t;
   s.t0 = t0;
   s.d0 = d0;
   s.K = K;
@@ -1455,12 +1492,12 @@ __device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const P
 // One work item: a whole row (part < 0) or part `part` of split row t, whose
 // index among the split rows is `split`. Returns false on a copy timeout.
 template <int DT, bool VEC>
-__device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int t, int part,
+__device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int o, int part,
                              int split) {
   const int tid = threadIdx.x;
-  if (tid < 32) row_meta(P, s, t);
+  if (tid < 32) row_meta(P, s, o);
   __syncthreads();
-  const int b = s.b, t0 = s.t0, d0 = s.d0, K = s.K, i = s.i;
+  const int b = s.b, t = s.t, t0 = s.t0, d0 = s.d0, K = s.K, i = s.i;
   const bool greedy = s.greedy != 0;
   const size_t rowb = (size_t)P.V * Elem<DT>::kBytes;
   const char* trow = static_cast<const char*>(P.target) + (size_t)t * rowb;
@@ -1531,6 +1568,7 @@ __global__ void __launch_bounds__(kThreads, SV_MINBLOCKS) verify_kernel(Params P
   }
   const unsigned R_t = (unsigned)(P.cu[P.B] + P.B);
   if (tid == 0) {
+    s.R_d = P.cu[P.B];
     // Work items: whole rows, then the last rows split into parts.
     unsigned W = 0, np = 1;
     if (VEC) {
