@@ -41,8 +41,8 @@ WORKLOAD = ("sampling verify B=256 K=7 V=151936 bf16 T=0.7, peaked rank-score ro
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per verify launch on this workload from one ncu
 # capture, valid only for the kernel sources whose hash is recorded with it.
-TRAFFIC = {"sources_sha256": "0d5792ca242477a800d78d3a955fd4708477a0977993fb0bea6e9fd89ff60465",
-           "bytes_per_launch": 1233614000 + 5711872,
+TRAFFIC = {"sources_sha256": "5eb80d66fd47183888fe31656b105c4a552e5b49418b5153f8daaf171d2fc9e2",
+           "bytes_per_launch": 1236312000 + 3829248,
            "profile": "profiles/verify_kernel_sampling_B256_K7_V151936_bf16.md"}
 
 
