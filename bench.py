@@ -385,6 +385,8 @@ EXTRA_WORKLOADS = {
                   "covering 30%, n=3, up to 5 tokens",
     "onehot_b128": "verify of the n-gram proposals (one-hot q), fp32 z ~ N(0,2^2), V=32000, T=1.0",
     "ragged_b512": "ragged mixed verify B=512 K_b~U{1..8} V=256000 bf16 T=1.0, half greedy requests",
+    "metrics_b512": "acceptance statistics of 512 verify rounds (K_b~U{1..8}) added to a device "
+                    "counter block",
 }
 
 
@@ -427,6 +429,34 @@ def _extra_setup(name, seed):
         desc = {"B": int(h.shape[0]), "L": int(nb.histories.shape[1]), "n": nb.max_n,
                 "max_tokens": nb.max_tokens}
         return (desc, host, outs, step, int(h.shape[0]), "histories/s", int(nb.histories.nbytes),
+                True, oracle_fn, check)
+
+    if name == "metrics_b512":
+        import oracle
+        rng = np.random.default_rng(seed)
+        B = 512
+        K = rng.integers(1, 9, size=B)
+        cu = np.concatenate([[0], np.cumsum(K)]).astype(np.int32)
+        lens = rng.integers(1, K + 2).astype(np.int32)
+        d_cu, d_len = torch.from_numpy(cu).cuda(), torch.from_numpy(lens).cuda()
+        m = api.new_metrics()
+        host = {"cu": (d_cu, torch.from_numpy(cu).pin_memory()),
+                "len": (d_len, torch.from_numpy(lens).pin_memory())}
+
+        def step():
+            api.sv_accumulate_metrics(d_cu, d_len, m)
+
+        def oracle_fn():
+            t = time.perf_counter()
+            o = oracle.acceptance_metrics(cu, lens)
+            return time.perf_counter() - t, 1, o
+
+        def check(o):
+            m1 = api.new_metrics()
+            api.sv_accumulate_metrics(d_cu, d_len, m1)
+            g = api.metrics_dict(m1)
+            return {"rounds": B, "bit_exact": all(g[k] == o[k] for k in o)}
+        return ({"B": B, "K": "U{1..8}"}, host, [m], step, B, "rounds/s", int(cu.nbytes + lens.nbytes),
                 True, oracle_fn, check)
 
     if name == "verify_b1":
@@ -557,20 +587,23 @@ def run_extra(args):
     line = {
         "metric": METRIC, "value": units / (ms * 1e-3), "unit": unit, "n_gpus": 1, "steps": n,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "i32" if args.workload == "ngram_b128" else "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "i32" if args.workload in ("ngram_b128", "metrics_b512") else "f32",
+        "data": "synthetic",
         "config": dict({"workload": EXTRA_WORKLOADS[args.workload],
                         "l2": "before each timed launch a 256 MB buffer is written and another "
                               "256 MB read (flush, clean lines)" if flush
                         else "inputs larger than L2: no flush"}, **desc),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
-                     "note": "latency-bound: one CTA per history" if args.workload == "ngram_b128" else None},
+                     "note": {"ngram_b128": "latency-bound: one CTA per history",
+                              "metrics_b512": "latency-bound: 4 KB of inputs"}.get(args.workload)},
         "e2e": {"value": units / (e_ms * 1e-3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e_ms},
         "gpu_launches": n,
         "clocks": clocks,
         "cpu_baseline": {"value": (units if args.workload in ("ngram_b128", "verify_b1", "greedy_b64",
-                                                            "onehot_b128") else spot["rows"]) / dt,
+                                                            "onehot_b128", "metrics_b512")
+                                   else spot["rows"]) / dt,
                          "unit": unit, "cores": threads, "kind": "oracle",
                          "sample": "the whole step" if args.workload != "ragged_b512" else "64 of 512 requests"},
         "parity_spot_check": spot,

@@ -237,6 +237,68 @@ sv_status sv_pack_drafts(const int32_t* tokens, const int32_t* counts, int32_t B
                          void* cuda_stream);
 
 /*
+ * Acceptance statistics ("5.2 Draft 模型与无模型方案", §7.1 and §7.2),
+ * accumulated on the device over any number of verify calls.
+ *
+ * sv_accumulate_metrics adds one call's rounds to *metrics (a DEVICE
+ * pointer to a caller-owned, 8-byte aligned sv_metrics that the caller
+ * zero-fills to start a window). It reads the call's cu_draft [B+1] and
+ * out_len [B] (device) after spec_verify / spec_verify_greedy has run on the
+ * same stream. Each request is one round. Its stop slot is out_len - 1
+ * (clamped to [0, K_b]): slots before it were accepted, the slot itself was
+ * rejected, or was the bonus slot. Asynchronous on `cuda_stream`;
+ * SV_ERR_INVALID_ARG for bad pointers or B < 0. Per-slot counts cover slots
+ * i < SV_METRICS_MAX_POS; the totals cover every slot.
+ *
+ * Quantities the pages define, from the counters:
+ *   draft acceptance rate      accepted / drafted            (C / D)
+ *   mean acceptance length     1 + accepted / rounds         (1 + C / R)
+ *   candidate coverage         rounds_with_draft / rounds
+ *   conditional rate of slot i accepted_at[i] / reached[i]   (given all before it)
+ *   rate through slot i        accepted_at[i] / offered[i]   (all of 0..i accepted)
+ */
+#define SV_METRICS_MAX_POS 32
+typedef struct {
+  unsigned long long rounds;            /* R: requests verified */
+  unsigned long long rounds_with_draft; /* rounds with K_b > 0 */
+  unsigned long long drafted;           /* D: sum of K_b */
+  unsigned long long accepted;          /* C: sum of stop slots (accepted draft tokens) */
+  unsigned long long committed;         /* sum of out_len = C + R */
+  unsigned long long offered[SV_METRICS_MAX_POS];     /* rounds with K_b > i */
+  unsigned long long reached[SV_METRICS_MAX_POS];     /* rounds that tested slot i */
+  unsigned long long accepted_at[SV_METRICS_MAX_POS]; /* rounds that accepted slots 0..i */
+} sv_metrics;
+sv_status sv_accumulate_metrics(const int32_t* cu_draft, const int32_t* out_len, int32_t B,
+                                sv_metrics* metrics, void* cuda_stream);
+
+/*
+ * Sliding-window draft-length controller ("投机解码从零实现", §5.2
+ * "动态草稿长度策略"), host code. Each round adds its accepted fraction
+ * accepted_len / max(draft_len, 1) to a window of the last `window` rounds.
+ * Once the window holds at least SV_ADAPT_MIN_ROUNDS rounds, every update
+ * compares the window's mean m with `target`:
+ *   - m > target + SV_ADAPT_BAND: the draft length grows by one, up to max_k;
+ *   - m < target - SV_ADAPT_BAND: it shrinks by one, down to min_k.
+ * The mean is summed oldest round first in double precision. One
+ * controller per request stream; the struct is plain data (copyable, no
+ * allocation). SV_ERR_INVALID_ARG for NULL, window outside
+ * [1, SV_ADAPT_MAX_WINDOW], k bounds out of order, or accepted_len outside
+ * [0, draft_len].
+ */
+#define SV_ADAPT_MAX_WINDOW 1024
+#define SV_ADAPT_MIN_ROUNDS 10
+#define SV_ADAPT_BAND 0.1
+typedef struct {
+  int32_t window, min_k, max_k, k, count, next;
+  double target;
+  double ratio[SV_ADAPT_MAX_WINDOW]; /* ring of accepted fractions */
+} sv_adapt;
+sv_status sv_adapt_init(sv_adapt* a, int32_t window, int32_t min_k, int32_t max_k, double target,
+                        int32_t initial_k);
+sv_status sv_adapt_update(sv_adapt* a, int32_t draft_len, int32_t accepted_len);
+int32_t sv_adapt_draft_length(const sv_adapt* a);
+
+/*
  * Synchronizes `cuda_stream`, reads the status word of `workspace` into
  * *out_bits (SV_DATA_* / SV_DEV_* bits) and clears it. Returns SV_OK when no
  * error bit is set (SV_DATA_DEGENERATE_RESIDUAL alone is informational),

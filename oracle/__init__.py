@@ -172,3 +172,79 @@ def ngram_propose(histories, hist_len, min_n: int, max_n: int, max_tokens: int):
     if st != 0:
         raise ValueError("oracle_ngram_propose: history length out of range")
     return out, cnt, nn
+
+
+# ---------------------------------------------------------------------------
+# Acceptance statistics and the draft-length controller (plain Python)
+# ---------------------------------------------------------------------------
+def acceptance_metrics(cu_draft, out_len, max_pos: int = 32) -> dict:
+    """Counts of "5.2 Draft 模型与无模型方案", §7.1-7.2, over the rounds of one
+    or more verify calls (each request is a round).
+
+    D: proposed draft tokens; C: accepted draft tokens, i.e. the tokens
+    committed from the draft before the first rejection (out_len - 1);
+    R: rounds. Per slot i: offered (K_b > i), reached (slot i was tested, so
+    every earlier slot was accepted) and accepted_at (slots 0..i accepted).
+    """
+    cu = [int(x) for x in cu_draft]
+    lens = [int(x) for x in out_len]
+    m = {"rounds": 0, "rounds_with_draft": 0, "drafted": 0, "accepted": 0, "committed": 0,
+         "offered": [0] * max_pos, "reached": [0] * max_pos, "accepted_at": [0] * max_pos}
+    for b in range(len(lens)):
+        K = max(0, cu[b + 1] - cu[b])
+        length = min(max(lens[b], 1), K + 1)
+        stop = length - 1  # slots 0..stop-1 accepted; slot stop rejected, or the bonus slot
+        m["rounds"] += 1
+        if K > 0:
+            m["rounds_with_draft"] += 1
+        m["drafted"] += K
+        m["accepted"] += stop
+        m["committed"] += length
+        for i in range(min(K, max_pos)):
+            m["offered"][i] += 1
+            if i <= stop:
+                m["reached"][i] += 1
+            if i < stop:
+                m["accepted_at"][i] += 1
+    return m
+
+
+def derived_rates(m: dict) -> dict:
+    """The page's quantities from the counts: C/D, 1 + C/R, coverage, and per
+    slot the conditional rate and the rate through that slot."""
+    R, D, C = m["rounds"], m["drafted"], m["accepted"]
+    return {
+        "draft_acceptance_rate": C / D if D else float("nan"),
+        "mean_acceptance_length": 1 + C / R if R else float("nan"),
+        "coverage": m["rounds_with_draft"] / R if R else float("nan"),
+        "conditional": [a / r if r else float("nan") for a, r in zip(m["accepted_at"], m["reached"])],
+        "through": [a / o if o else float("nan") for a, o in zip(m["accepted_at"], m["offered"])],
+    }
+
+
+class AdaptiveDraftLength:
+    """Sliding-window draft-length rule of "投机解码从零实现" §5.2
+    (动态草稿长度策略): keep the accepted fraction of the last `window`
+    rounds; from 10 rounds on, after each round move the draft length one
+    step up when the window's mean exceeds target + 0.1, one step down when
+    it falls below target - 0.1, within [min_k, max_k]."""
+
+    def __init__(self, window=100, min_k=1, max_k=10, target=0.7, initial_k=5):
+        self.window, self.min_k, self.max_k, self.target = window, min_k, max_k, float(target)
+        self.k = initial_k
+        self.fractions = []
+
+    def update(self, draft_len: int, accepted_len: int) -> int:
+        self.fractions.append(accepted_len / max(draft_len, 1))
+        if len(self.fractions) > self.window:
+            self.fractions = self.fractions[1:]
+        if len(self.fractions) >= 10:
+            total = 0.0
+            for f in self.fractions:  # oldest first
+                total += f
+            mean = total / len(self.fractions)
+            if mean > self.target + 0.1:
+                self.k = min(self.max_k, self.k + 1)
+            elif mean < self.target - 0.1:
+                self.k = max(self.min_k, self.k - 1)
+        return self.k

@@ -230,3 +230,71 @@ def sv_check_status(workspace: torch.Tensor, stream=None) -> int:
     if st not in (SV_OK, SV_ERR_DATA, SV_ERR_TIMEOUT):
         raise SpecVerifyError("sv_check_status", st)
     return int(bits.value)
+
+
+# ---------------------------------------------------------------------------
+# Acceptance statistics and the draft-length controller
+# ---------------------------------------------------------------------------
+SV_METRICS_MAX_POS = 32
+_METRIC_SCALARS = ("rounds", "rounds_with_draft", "drafted", "accepted", "committed")
+_METRIC_WORDS = len(_METRIC_SCALARS) + 3 * SV_METRICS_MAX_POS
+
+
+def new_metrics(device="cuda") -> torch.Tensor:
+    """A zeroed sv_metrics block on the device (64-bit counters)."""
+    return torch.zeros(_METRIC_WORDS, dtype=torch.int64, device=device)
+
+
+def sv_accumulate_metrics(cu_draft: torch.Tensor, out_len: torch.Tensor, metrics: torch.Tensor,
+                          stream=None) -> torch.Tensor:
+    """Adds one verify call's rounds to `metrics` (see new_metrics)."""
+    lib = load()
+    fn = lib.sv_accumulate_metrics
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    if metrics.numel() != _METRIC_WORDS or metrics.dtype != torch.int64:
+        raise ValueError("metrics must come from new_metrics()")
+    _check("sv_accumulate_metrics", fn(_ptr(cu_draft), _ptr(out_len), int(out_len.numel()),
+                                       _ptr(metrics), _stream(stream)))
+    return metrics
+
+
+def metrics_dict(metrics: torch.Tensor) -> dict:
+    """The counters as a host dict (keys as in the header's sv_metrics)."""
+    v = [int(x) for x in metrics.cpu().tolist()]
+    d = dict(zip(_METRIC_SCALARS, v[:5]))
+    P = SV_METRICS_MAX_POS
+    d["offered"], d["reached"], d["accepted_at"] = v[5:5 + P], v[5 + P:5 + 2 * P], v[5 + 2 * P:5 + 3 * P]
+    return d
+
+
+class _Adapt(ctypes.Structure):
+    _fields_ = [("window", ctypes.c_int32), ("min_k", ctypes.c_int32), ("max_k", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("count", ctypes.c_int32), ("next", ctypes.c_int32),
+                ("target", ctypes.c_double), ("ratio", ctypes.c_double * 1024)]
+
+
+class AdaptiveDraftLength:
+    """The library's sliding-window draft-length controller (host code)."""
+
+    def __init__(self, window=100, min_k=1, max_k=10, target=0.7, initial_k=5):
+        lib = load()
+        lib.sv_adapt_init.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_double, ctypes.c_int32]
+        lib.sv_adapt_init.restype = ctypes.c_int
+        lib.sv_adapt_update.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32]
+        lib.sv_adapt_update.restype = ctypes.c_int
+        lib.sv_adapt_draft_length.argtypes = [ctypes.c_void_p]
+        lib.sv_adapt_draft_length.restype = ctypes.c_int32
+        self._lib = lib
+        self._s = _Adapt()
+        _check("sv_adapt_init", lib.sv_adapt_init(ctypes.byref(self._s), window, min_k, max_k,
+                                                  float(target), initial_k))
+
+    def update(self, draft_len: int, accepted_len: int) -> int:
+        _check("sv_adapt_update", self._lib.sv_adapt_update(ctypes.byref(self._s), draft_len, accepted_len))
+        return self.draft_length
+
+    @property
+    def draft_length(self) -> int:
+        return int(self._lib.sv_adapt_draft_length(ctypes.byref(self._s)))

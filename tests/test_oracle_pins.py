@@ -369,3 +369,69 @@ def test_ngram_bruteforce(oracle_mod):
         out, cnt, n = oracle_mod.ngram_propose(hb, [L], min_n, max_n, mt)
         en, ed = _ngram_naive(h, min_n, max_n, mt)
         assert n[0] == en and list(out[0, :cnt[0]]) == ed, (h, min_n, max_n, mt)
+
+
+# --------------------------------------------------------------------------
+# Acceptance statistics ("5.2 Draft 模型与无模型方案", §7.1-7.2)
+# --------------------------------------------------------------------------
+def test_acceptance_metrics_worked_example(oracle_mod):
+    import json
+    g = json.load(open(os.path.join(GOLDEN, "acceptance_metrics.json")))
+    m = oracle_mod.acceptance_metrics(g["cu_draft"], g["out_len"], max_pos=3)
+    e = g["expect"]
+    for k in ("rounds", "rounds_with_draft", "drafted", "accepted", "committed", "offered", "reached",
+              "accepted_at"):
+        assert m[k] == e[k], k
+    r = oracle_mod.derived_rates(m)
+    assert r["draft_acceptance_rate"] == e["draft_acceptance_rate"]
+    assert r["mean_acceptance_length"] == e["mean_acceptance_length"]
+    assert abs(r["coverage"] - e["coverage"]) < 1e-15
+    for got, want in zip(r["conditional"], e["conditional"]):
+        assert (want is None and got != got) or got == want
+    assert r["through"] == e["through"]
+
+
+def test_acceptance_metrics_identities(oracle_mod):
+    """committed = C + R; fixed gamma (D = gamma R) gives 1 + C/R = 1 + gamma C/D
+    (§7.2); the rate through slot i never exceeds the conditional rate, and
+    reached[i+1] = accepted_at[i] for rounds that propose slot i+1."""
+    rng = np.random.default_rng(3)
+    gamma, B = 5, 400
+    cu = np.arange(B + 1) * gamma
+    lens = rng.integers(1, gamma + 2, size=B)
+    m = oracle_mod.acceptance_metrics(cu, lens)
+    r = oracle_mod.derived_rates(m)
+    assert m["committed"] == m["accepted"] + m["rounds"]
+    assert m["drafted"] == gamma * m["rounds"]
+    assert abs(r["mean_acceptance_length"] - (1 + gamma * m["accepted"] / m["drafted"])) < 1e-12
+    for i in range(gamma - 1):
+        assert m["reached"][i + 1] == m["accepted_at"][i]
+    for i in range(gamma):
+        assert r["through"][i] <= r["conditional"][i] + 1e-15
+    # accepted counts: sum over slots of accepted_at equals C
+    assert sum(m["accepted_at"]) == m["accepted"]
+
+
+# --------------------------------------------------------------------------
+# Draft-length controller ("投机解码从零实现", §5.2 动态草稿长度策略)
+# --------------------------------------------------------------------------
+def test_controller_waits_for_ten_rounds_then_steps_to_the_bounds(oracle_mod):
+    c = oracle_mod.AdaptiveDraftLength(window=100, min_k=1, max_k=10, target=0.7, initial_k=5)
+    ks = [c.update(4, 4) for _ in range(15)]           # every proposal accepted
+    assert ks == [5] * 9 + [6, 7, 8, 9, 10, 10]
+    c = oracle_mod.AdaptiveDraftLength(window=100, min_k=2, max_k=10, target=0.7, initial_k=5)
+    ks = [c.update(4, 0) for _ in range(14)]           # every proposal rejected
+    assert ks == [5] * 9 + [4, 3, 2, 2, 2]
+    c = oracle_mod.AdaptiveDraftLength(window=100, min_k=1, max_k=10, target=0.7, initial_k=5)
+    assert [c.update(10, 7) for _ in range(30)] == [5] * 30   # on target: no move
+    c = oracle_mod.AdaptiveDraftLength(window=100, min_k=1, max_k=10, target=0.7, initial_k=5)
+    assert [c.update(0, 0) for _ in range(12)] == [5] * 9 + [4, 3, 2]  # no proposal counts as 0
+
+
+def test_controller_window_forgets_old_rounds(oracle_mod):
+    """window 10, target 0.65 (band 0.55..0.75): ten all-accepted rounds, then
+    all-rejected ones; after n of those the window mean is (10 - n) / 10."""
+    c = oracle_mod.AdaptiveDraftLength(window=10, min_k=1, max_k=10, target=0.65, initial_k=5)
+    ks = [c.update(3, 3) for _ in range(10)] + [c.update(3, 0) for _ in range(10)]
+    # means 0.9, 0.8 raise; 0.7, 0.6 hold; 0.5 .. 0.0 lower
+    assert ks == [5] * 9 + [6] + [7, 8, 8, 8, 7, 6, 5, 4, 3, 2]
