@@ -59,6 +59,11 @@ def _load():
         lib.oracle_spec_verify.argtypes = [P, P, i32, i32, i32, P, P, P, P, f64,
                                            P, P, P, P, P, P, i32]
         lib.oracle_spec_verify.restype = i32
+        lib.oracle_spec_verify_filtered.argtypes = [P, P, i32, i32, i32, P, P, P, P, f64, i32, f64,
+                                                    P, P, P, P, P, P, i32]
+        lib.oracle_spec_verify_filtered.restype = i32
+        lib.oracle_filtered_softmax.argtypes = [P, i32, i32, f64, i32, f64, P, P]
+        lib.oracle_filtered_softmax.restype = f64
         lib.oracle_ngram_propose.argtypes = [P, i64, P, i32, i32, i32, i32, P, P, P]
         lib.oracle_ngram_propose.restype = i32
         lib.oracle_default_threads.argtypes = []
@@ -120,14 +125,29 @@ class VerifyResult:
         return self.margin < MARGIN_EPS
 
 
+def filtered_softmax(row, temperature: float, top_k: int = 0, top_p: float = 1.0):
+    """(p, top-p decision margin) of one logit row under the top-k / top-p
+    filters (oracle.c, oracle_filtered_softmax)."""
+    row, dt = _logits(np.asarray(row)[None, :] if np.asarray(row).ndim == 1 else row)
+    V = row.shape[-1]
+    p = np.zeros(V, np.float64)
+    m = ctypes.c_double(0.0)
+    _load().oracle_filtered_softmax(_ptr(row), dt, V, float(temperature), int(top_k), float(top_p),
+                                    _ptr(p), ctypes.byref(m))
+    return p, m.value
+
+
 def spec_verify(target, draft, draft_tokens, cu_draft, uniforms, temperature: float,
-                mode=None, nthreads: int = 0, diagnostics: bool = True) -> VerifyResult:
+                mode=None, nthreads: int = 0, diagnostics: bool = True, top_k: int = 0,
+                top_p: float = 1.0) -> VerifyResult:
     """Verify-and-commit for a packed batch (layout as the CUDA library's).
 
     target: [R_t, V] float32 or uint16(bf16); draft: [R_d, V] same dtype or None
     (one-hot q); draft_tokens: [R_d] int32; cu_draft: [B+1] int32; uniforms:
     [R_t, 2] float32; mode: [B] uint8 (0 sample, 1 greedy) or None. diagnostics=False skips the
     per-row (p(x̂), q(x̂)) outputs, leaving only the method's own work.
+    top_k / top_p (0 / 1.0: off) filter the target and draft distributions
+    alike before the step (oracle.c, oracle_filtered_softmax).
     """
     target, dt = _logits(target)
     V = target.shape[-1]
@@ -148,9 +168,9 @@ def spec_verify(target, draft, draft_tokens, cu_draft, uniforms, temperature: fl
     margin = np.full(R_t, np.inf, np.float64)
     rho = np.full(R_t, np.nan, np.float64)
     stop = np.zeros(B, np.int32)
-    st = _load().oracle_spec_verify(
+    st = _load().oracle_spec_verify_filtered(
         _ptr(target), _ptr(draft), dt, V, B, _ptr(draft_tokens), _ptr(cu_draft), _ptr(mode),
-        _ptr(uniforms), float(temperature), _ptr(out_tokens), _ptr(out_len),
+        _ptr(uniforms), float(temperature), int(top_k), float(top_p), _ptr(out_tokens), _ptr(out_len),
         _ptr(out_probs) if diagnostics else None, _ptr(margin), _ptr(rho), _ptr(stop), int(nthreads))
     if st != 0:
         raise ValueError(f"oracle_spec_verify: invalid request data (code {st})")

@@ -124,6 +124,81 @@ double oracle_softmax(const void* row, int dtype, int V, double T, double* p) {
   return S;
 }
 
+/* Top-k / top-p filtered temperature softmax (the filters that
+ * "投机解码从零实现" §5.4 lists as distribution-preserving verify
+ * strategies; the same filter is applied to the target and the draft row).
+ * Readings, in this order:
+ *   top-k (1 <= top_k < V): keep every x whose logit is >= the k-th largest
+ *     logit (ties at the boundary are all kept);
+ *   top-p (0 < top_p < 1): on the renormalised top-k distribution, walk the
+ *     distinct kept values from the largest down; keep the values whose
+ *     cumulative mass first reaches top_p (a value's whole tie group counts
+ *     together), drop the rest.
+ * p receives the renormalised filtered distribution. *margin receives the
+ * distance of the top-p decision from equality, min(top_p - C_before,
+ * C_at - top_p) in normalised mass (+inf when top-p is off). Returns the
+ * unfiltered normaliser as oracle_softmax does (0: no finite logit). */
+static int cmp_desc(const void* a, const void* b) {
+  double x = *(const double*)a, y = *(const double*)b;
+  return x < y ? 1 : (x > y ? -1 : 0);
+}
+
+double oracle_filtered_softmax(const void* row, int dtype, int V, double T, int top_k,
+                               double top_p, double* p, double* margin) {
+  if (margin) *margin = INFINITY;
+  const int use_k = top_k >= 1 && top_k < V;
+  const int use_p = top_p > 0.0 && top_p < 1.0;
+  double S_all = oracle_softmax(row, dtype, V, T, p);
+  if (!(S_all > 0.0) || (!use_k && !use_p)) return S_all;
+  double* z = (double*)malloc(sizeof(double) * (size_t)V);
+  double* sorted = (double*)malloc(sizeof(double) * (size_t)V);
+  if (!z || !sorted) {
+    free(z);
+    free(sorted);
+    return -1.0;
+  }
+  for (int x = 0; x < V; ++x) z[x] = sorted[x] = logit_at(row, dtype, x);
+  qsort(sorted, (size_t)V, sizeof(double), cmp_desc);
+  const double m = sorted[0];
+  double thr = use_k ? sorted[top_k - 1] : -INFINITY;
+  if (use_p) {
+    /* Mass of the top-k set, then the cumulative mass by distinct value. */
+    nsum_t tot = {0.0, 0.0};
+    for (int x = 0; x < V; ++x)
+      if (z[x] >= thr) nsum_add(&tot, exp((z[x] - m) / T));
+    const double S_k = nsum_value(&tot);
+    nsum_t cum = {0.0, 0.0};
+    double before = 0.0;
+    int j = 0;
+    while (j < V && sorted[j] >= thr) {
+      const double v = sorted[j];
+      int g = j;
+      while (g < V && sorted[g] == v) {
+        nsum_add(&cum, exp((v - m) / T));
+        ++g;
+      }
+      const double at = nsum_value(&cum) / S_k;
+      if (at >= top_p) {
+        if (margin) *margin = fmin(top_p - before, at - top_p);
+        if (v > thr) thr = v;
+        break;
+      }
+      before = at;
+      j = g;
+    }
+  }
+  nsum_t s = {0.0, 0.0};
+  for (int x = 0; x < V; ++x) {
+    p[x] = z[x] >= thr ? exp((z[x] - m) / T) : 0.0;
+    nsum_add(&s, p[x]);
+  }
+  const double S = nsum_value(&s);
+  for (int x = 0; x < V; ++x) p[x] /= S;
+  free(z);
+  free(sorted);
+  return S_all;
+}
+
 /* Greedy choice of the target: the first index holding the maximum
  * (torch.argmax semantics), compared on the exact logit values. */
 int oracle_argmax(const void* row, int dtype, int V) {
@@ -193,6 +268,8 @@ typedef struct {
   double* out_margin;          /* [R_t] or NULL: smallest decision margin per row */
   double* out_rho;             /* [R_t] or NULL: min(1, p/q) per tested row */
   int32_t* out_stop;           /* [B] or NULL */
+  int top_k;                   /* 0: off */
+  double top_p;                /* >= 1: off */
 } verify_args_t;
 
 static const void* row_ptr(const void* base, int dtype, int64_t row, int V) {
@@ -202,6 +279,14 @@ static const void* row_ptr(const void* base, int dtype, int64_t row, int V) {
 
 static void set_margin(const verify_args_t* a, int64_t t, double m) {
   if (a->out_margin && m < a->out_margin[t]) a->out_margin[t] = m;
+}
+
+/* Softmax of a target or draft row with the call's filters; the top-p
+ * decision margin is charged to target row t (the row of that slot). */
+static void row_softmax(const verify_args_t* a, const void* row, double* p, int64_t t) {
+  double fm = INFINITY;
+  oracle_filtered_softmax(row, a->dtype, a->V, a->T, a->top_k, a->top_p, p, &fm);
+  set_margin(a, t, fm);
 }
 
 /* Returns 0 on success, nonzero on invalid data for this request. */
@@ -232,10 +317,10 @@ static int verify_request(const verify_args_t* a, int b, double* p, double* q,
         continue;
       }
       int x = a->draft_tokens[d0 + i];
-      oracle_softmax(row_ptr(a->target, a->dtype, t0 + i, V), a->dtype, V, a->T, p);
+      row_softmax(a, row_ptr(a->target, a->dtype, t0 + i, V), p, t0 + i);
       o[0] = p[x];
       if (a->draft) {
-        oracle_softmax(row_ptr(a->draft, a->dtype, d0 + i, V), a->dtype, V, a->T, q);
+        row_softmax(a, row_ptr(a->draft, a->dtype, d0 + i, V), q, t0 + i);
         o[1] = q[x];
       } else {
         o[1] = 1.0;
@@ -253,10 +338,10 @@ static int verify_request(const verify_args_t* a, int b, double* p, double* q,
       /* [DSD-2] strict: accept iff the draft equals the target's choice. */
       accept = (x == oracle_argmax(row_ptr(a->target, a->dtype, t, V), a->dtype, V));
     } else {
-      oracle_softmax(row_ptr(a->target, a->dtype, t, V), a->dtype, V, a->T, p);
+      row_softmax(a, row_ptr(a->target, a->dtype, t, V), p, t);
       double ph = p[x], qh;
       if (a->draft) {
-        oracle_softmax(row_ptr(a->draft, a->dtype, d0 + i, V), a->dtype, V, a->T, q);
+        row_softmax(a, row_ptr(a->draft, a->dtype, d0 + i, V), q, t);
         qh = q[x];
       } else {
         qh = 1.0; /* [PL-4.3] one-hot proposal */
@@ -285,13 +370,13 @@ static int verify_request(const verify_args_t* a, int b, double* p, double* q,
   if (greedy) {
     y = oracle_argmax(row_ptr(a->target, a->dtype, s, V), a->dtype, V);
   } else {
-    oracle_softmax(row_ptr(a->target, a->dtype, s, V), a->dtype, V, a->T, p);
+    row_softmax(a, row_ptr(a->target, a->dtype, s, V), p, s);
     int have_q = 0;
     if (stop < K) {
       const int x = a->draft_tokens[d0 + stop];
       if (a->draft) {
         /* [DM-rule], [SDS-3.2]: r = max(0, p - q). */
-        oracle_softmax(row_ptr(a->draft, a->dtype, d0 + stop, V), a->dtype, V, a->T, q);
+        row_softmax(a, row_ptr(a->draft, a->dtype, d0 + stop, V), q, s);
         for (int k = 0; k < V; ++k) r[k] = p[k] > q[k] ? p[k] - q[k] : 0.0;
         have_q = 1;
       } else {
@@ -365,15 +450,15 @@ int oracle_default_threads(void) { return resolve_threads(0); }
  * error code (1: negative draft count, 2: draft token out of range,
  * -1: out of memory).
  */
-int oracle_spec_verify(const void* target, const void* draft, int dtype, int V, int B,
-                       const int32_t* draft_tokens, const int32_t* cu_draft,
-                       const uint8_t* mode, const float* uniforms, double T,
-                       int32_t* out_tokens, int32_t* out_len, double* out_probs,
-                       double* out_margin, double* out_rho, int32_t* out_stop,
-                       int nthreads) {
-  verify_args_t a = {target, draft,  dtype,      V,          B,         draft_tokens,
-                     cu_draft, mode, uniforms, T, out_tokens, out_len, out_probs,
-                     out_margin, out_rho, out_stop};
+int oracle_spec_verify_filtered(const void* target, const void* draft, int dtype, int V, int B,
+                                const int32_t* draft_tokens, const int32_t* cu_draft,
+                                const uint8_t* mode, const float* uniforms, double T,
+                                int top_k, double top_p, int32_t* out_tokens, int32_t* out_len,
+                                double* out_probs, double* out_margin, double* out_rho,
+                                int32_t* out_stop, int nthreads) {
+  verify_args_t a = {target,     draft,   dtype,     V,         B,        draft_tokens,
+                     cu_draft,   mode,    uniforms,  T,         out_tokens, out_len,
+                     out_probs,  out_margin, out_rho, out_stop, top_k,    top_p};
   if (B <= 0) return 0;
   int nt = resolve_threads(nthreads);
   if (nt > B) nt = B;
@@ -397,6 +482,18 @@ int oracle_spec_verify(const void* target, const void* draft, int dtype, int V, 
   free(jobs);
   free(th);
   return status;
+}
+
+/* Unfiltered form (the method as the algorithm box gives it). */
+int oracle_spec_verify(const void* target, const void* draft, int dtype, int V, int B,
+                       const int32_t* draft_tokens, const int32_t* cu_draft,
+                       const uint8_t* mode, const float* uniforms, double T,
+                       int32_t* out_tokens, int32_t* out_len, double* out_probs,
+                       double* out_margin, double* out_rho, int32_t* out_stop,
+                       int nthreads) {
+  return oracle_spec_verify_filtered(target, draft, dtype, V, B, draft_tokens, cu_draft, mode,
+                                     uniforms, T, 0, 1.0, out_tokens, out_len, out_probs,
+                                     out_margin, out_rho, out_stop, nthreads);
 }
 
 /* ------------------------------------------------------------------ */

@@ -435,3 +435,82 @@ def test_controller_window_forgets_old_rounds(oracle_mod):
     ks = [c.update(3, 3) for _ in range(10)] + [c.update(3, 0) for _ in range(10)]
     # means 0.9, 0.8 raise; 0.7, 0.6 hold; 0.5 .. 0.0 lower
     assert ks == [5] * 9 + [6] + [7, 8, 8, 8, 7, 6, 5, 4, 3, 2]
+
+
+# --------------------------------------------------------------------------
+# Top-k / top-p filtered verify ("投机解码从零实现" §5.4: top-k and nucleus
+# rejection sampling keep the distribution; the same filter on p and q)
+# --------------------------------------------------------------------------
+LN2_T = 1.0 / np.log(2.0)  # with T = 1/ln 2, exp(z / T) = 2^z exactly for these logits
+
+
+def test_filters_closed_forms(oracle_mod):
+    z = np.array([2, 1, 0, -1, -3], np.float32)  # weights 4, 2, 1, 1/2, 1/8
+    w = np.array([4, 2, 1, 0.5, 0.125])
+    cases = [  # (top_k, top_p, kept)
+        (0, 1.0, 5), (5, 1.0, 5), (2, 1.0, 2), (1, 1.0, 1),
+        (0, 0.5, 1),     # 4/7.625 = 0.5246 >= 0.5
+        (0, 0.53, 2),    # 0.5246 < 0.53 <= 6/7.625
+        (0, 0.90, 3),    # 6/7.625 = 0.787 < 0.90 <= 7/7.625 = 0.918
+        (3, 0.90, 3),    # on the top-3 renormalised: 4/7, 6/7 < 0.9 <= 1
+        (4, 0.80, 3),    # top-4 total 7.5: 6/7.5 = 0.8 reaches 0.80 exactly? see margin test
+    ]
+    for k, pp, kept in cases[:-1]:
+        p, m = oracle_mod.filtered_softmax(z, LN2_T, k, pp)
+        want = np.where(np.arange(5) < kept, w, 0.0)
+        want = want / want.sum()
+        assert np.allclose(p, want, rtol=0, atol=1e-14), (k, pp, p)
+        assert (m == np.inf) == (pp >= 1.0)
+
+
+def test_filters_keep_tie_groups_whole(oracle_mod):
+    p, _ = oracle_mod.filtered_softmax(np.array([1, 1, 1, 0], np.float32), LN2_T, 2, 1.0)
+    assert np.allclose(p, [1 / 3, 1 / 3, 1 / 3, 0], atol=1e-15)      # k-th largest is tied
+    p, _ = oracle_mod.filtered_softmax(np.array([1, 0, 1, -1], np.float32), LN2_T, 0, 0.3)
+    assert np.allclose(p, [0.5, 0, 0.5, 0], atol=1e-15)              # first group already > 0.3
+    p, _ = oracle_mod.filtered_softmax(np.array([-np.inf, 3, -np.inf, 2], np.float32), LN2_T, 3, 1.0)
+    assert np.allclose(p, [0, 2 / 3, 0, 1 / 3], atol=1e-15)          # -inf never kept in mass
+
+
+def test_filters_margin_flags_near_equal_boundary(oracle_mod):
+    z = np.array([2, 1, 0, -1, -3], np.float32)
+    # top-4 mass 7.5; the first two values carry 6/7.5 = 0.8 exactly
+    _, m = oracle_mod.filtered_softmax(z, LN2_T, 4, 0.8)
+    assert m < 1e-12
+    _, m = oracle_mod.filtered_softmax(z, LN2_T, 4, 0.75)
+    assert abs(m - 0.05) < 1e-12     # 4/7.5 = 0.5333 < 0.75 <= 0.8
+
+
+def test_filters_off_is_the_unfiltered_oracle(oracle_mod):
+    b = W.gaussian_sampling(seed=41, B=20, K=4, V=300, sigma=2.0, draft_sigma=0.7, T=0.8)
+    r0 = oracle_mod.spec_verify(b.target, b.draft, b.draft_tokens, b.cu_draft, b.uniforms, b.temperature)
+    r1 = oracle_mod.spec_verify(b.target, b.draft, b.draft_tokens, b.cu_draft, b.uniforms, b.temperature,
+                                top_k=300, top_p=1.0)
+    assert np.array_equal(r0.out_tokens, r1.out_tokens) and np.array_equal(r0.out_len, r1.out_len)
+    assert np.array_equal(r0.out_probs, r1.out_probs, equal_nan=True)
+
+
+def test_filtered_verify_is_lossless_for_the_filtered_target(oracle_mod):
+    """V=16, K=1, top-k 9 then top-p 0.85 on both rows; x̂ ~ q' (the filtered
+    draft); over 1e6 rounds the first emitted token follows p' (chi-square)."""
+    rng = np.random.default_rng(17)
+    V, N, k, pp = 16, 1_000_000, 9, 0.85
+    zp = rng.normal(0, 1.5, V).astype(np.float32)
+    zq = (zp + rng.normal(0, 1.0, V)).astype(np.float32)
+    zb = rng.normal(0, 1.5, V).astype(np.float32)
+    p1, _ = oracle_mod.filtered_softmax(zp, 1.0, k, pp)
+    q1, _ = oracle_mod.filtered_softmax(zq, 1.0, k, pp)
+    cu = np.arange(N + 1, dtype=np.int32)
+    x = np.searchsorted(np.cumsum(q1), rng.random(N), side="right").clip(0, V - 1).astype(np.int32)
+    target = np.tile(np.stack([zp, zb]), (N, 1))
+    draft = np.tile(zq[None], (N, 1))
+    r = oracle_mod.spec_verify(target, draft, x, cu, W.uniforms_for(cu, seed=23), 1.0, diagnostics=False,
+                               top_k=k, top_p=pp)
+    first = r.out_tokens.reshape(N, 2)[:, 0]
+    hist = np.bincount(first, minlength=V)
+    keep = p1 > 0
+    assert hist[~keep].sum() == 0
+    chi2 = float(((hist[keep] - N * p1[keep]) ** 2 / (N * p1[keep])).sum())
+    dof = int(keep.sum()) - 1
+    from scipy.stats import chi2 as chi2_dist
+    assert chi2 < chi2_dist.ppf(0.999, dof), (chi2, dof)
