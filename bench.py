@@ -387,7 +387,10 @@ EXTRA_WORKLOADS = {
     "ragged_b512": "ragged mixed verify B=512 K_b~U{1..8} V=256000 bf16 T=1.0, half greedy requests",
     "metrics_b512": "acceptance statistics of 512 verify rounds (K_b~U{1..8}) added to a device "
                     "counter block",
+    "topkp_b256": "top-k 50 / top-p 0.9 filtered sampling verify on the benchmark batch (B=256 K=7 "
+                  "V=151936 bf16 T=0.7, peaked rank-score rows)",
 }
+FILTER_K, FILTER_P = 50, 0.9
 
 
 def _extra_setup(name, seed):
@@ -470,6 +473,8 @@ def _extra_setup(name, seed):
         batches = [W.config4_verify(seed=seed, proposals=o[0], counts=o[1])]
     elif name == "ragged_b512":
         batches = [W.config5(seed=seed)]
+    elif name == "topkp_b256":
+        batches = [W.config3(seed=seed)]
     else:
         raise SystemExit(f"unknown workload {name}")
     dbs = [parity.to_device(b) for b in batches]
@@ -481,11 +486,19 @@ def _extra_setup(name, seed):
     op = torch.empty((R_t, 2), dtype=torch.float32, device="cuda")
     k = [0]
     greedy_only = name == "greedy_b64"
+    filtered = name == "topkp_b256"
+    if filtered:
+        ws = torch.zeros(api.spec_verify_filtered_workspace_size(b0.B, b0.R_t, b0.V), dtype=torch.uint8,
+                         device="cuda")
 
     def step():
         db = dbs[k[0] % len(dbs)]
         k[0] += 1
-        if greedy_only:
+        if filtered:
+            api.spec_verify_filtered(db.target, db.draft, db.draft_tokens, db.cu_draft, db.uniforms,
+                                     db.temperature, FILTER_K, FILTER_P, db.mode, out_tokens=ot, out_len=ol,
+                                     out_probs=op, workspace=ws)
+        elif greedy_only:
             api.spec_verify_greedy(db.target, db.draft_tokens, db.cu_draft, out_tokens=ot, out_len=ol,
                                    workspace=ws)
         else:
@@ -502,7 +515,14 @@ def _extra_setup(name, seed):
         reps = 200 if name == "verify_b1" else 1
         t = time.perf_counter()
         for _ in range(reps):
-            _, threads, res = time_oracle(sample, diagnostics=True)
+            if filtered:
+                import oracle
+                threads = min(oracle.default_threads(), sample.B)
+                res = oracle.spec_verify(sample.target, sample.draft, sample.draft_tokens, sample.cu_draft,
+                                         sample.uniforms, sample.temperature, sample.mode, threads,
+                                         top_k=FILTER_K, top_p=FILTER_P)
+            else:
+                _, threads, res = time_oracle(sample, diagnostics=True)
         return (time.perf_counter() - t) / reps, threads, res
 
     def check(res):
@@ -517,7 +537,10 @@ def _extra_setup(name, seed):
     nbytes = sum(b.algorithmic_bytes() for b in batches) / len(batches)
     desc = {"B": b0.B, "V": b0.V, "R_t": b0.R_t, "R_d": b0.R_d, "logits": "bf16" if b0.elem_bytes == 2 else "fp32",
             "temperature": b0.temperature, "input_sets": len(batches)}
-    return desc, host, [ot, ol], step, units, "rows/s", nbytes, name != "ragged_b512", oracle_fn, check
+    if filtered:
+        desc.update({"top_k": FILTER_K, "top_p": FILTER_P})
+    return desc, host, [ot, ol], step, units, "rows/s", nbytes, name not in ("ragged_b512", "topkp_b256"), \
+        oracle_fn, check
 
 
 def run_extra(args):
@@ -605,7 +628,8 @@ def run_extra(args):
                                                             "onehot_b128", "metrics_b512")
                                    else spot["rows"]) / dt,
                          "unit": unit, "cores": threads, "kind": "oracle",
-                         "sample": "the whole step" if args.workload != "ragged_b512" else "64 of 512 requests"},
+                         "sample": {"ragged_b512": "64 of 512 requests",
+                                    "topkp_b256": "64 of 256 requests"}.get(args.workload, "the whole step")},
         "parity_spot_check": spot,
     }
     print(json.dumps(line))

@@ -156,6 +156,45 @@ sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype, int32_t 
                              size_t workspace_bytes, void* cuda_stream);
 
 /*
+ * Top-k / top-p filtered verify-and-commit ("投机解码从零实现", §5.4
+ * "采样策略对比": top-k and nucleus rejection sampling keep the output
+ * distribution when the same filter is applied to the target and the draft
+ * distributions). Before the step, each sampled target row and draft row is
+ * filtered, then renormalised:
+ *   top_k (1 <= top_k < V; 0 or >= V: off): keep every token whose logit is
+ *     >= the row's k-th largest logit (ties at the boundary are all kept);
+ *   then top_p (0 < top_p < 1; >= 1: off): over the kept tokens, walk the
+ *     distinct logit values from the largest down and keep them until the
+ *     cumulative mass first reaches top_p; the last value's whole tie group
+ *     is kept, the rest dropped.
+ * The accept test, the residual max(0, p' - q') and the bonus draw then use
+ * the filtered p' and q'. The step is lossless with respect to the filtered
+ * target p' when the proposals were drawn from the filtered q'. One-hot
+ * proposals (draft_logits NULL) filter the target rows only. Greedy
+ * requests are unaffected, since a filter never removes the argmax.
+ *
+ * Arguments as for spec_verify, plus:
+ *   R_t        target rows the caller holds (cu_draft[B] + B); the
+ *              thresholds occupy the start of the workspace.
+ *   top_k, top_p  the filters (top_k >= 0, top_p > 0).
+ *   workspace  >= spec_verify_filtered_workspace_size(B, R_t, V) bytes,
+ *              16-byte aligned, zero-filled before first use.
+ * Per row, a threshold kernel runs a radix select on order-preserving keys
+ * (counts for top-k, masses 2^(z c - M c) summed in fp32 per warp for top-p),
+ * then the verify kernel runs with every logit below its row's threshold
+ * counted as -inf. A top-p decision within about 1e-6 of its boundary can
+ * differ from a float64 evaluation.
+ */
+size_t spec_verify_filtered_workspace_size(int32_t B, int32_t R_t, int32_t V);
+sv_status spec_verify_filtered(const void* target_logits, const void* draft_logits,
+                               sv_dtype dtype, int32_t V, int32_t B, int32_t R_t,
+                               const int32_t* draft_tokens, const int32_t* cu_draft,
+                               const uint8_t* mode, const float* uniforms, float temperature,
+                               int32_t top_k, float top_p, int32_t* out_tokens,
+                               int32_t* out_len, float* out_probs, void* workspace,
+                               size_t workspace_bytes, void* cuda_stream);
+
+/*
  * spec_verify without a caller workspace: the scratch memory lives in a
  * fixed block that is part of the library's device image, so the call
  * allocates nothing and takes no workspace argument. The pages have no

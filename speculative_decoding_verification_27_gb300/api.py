@@ -298,3 +298,46 @@ class AdaptiveDraftLength:
     @property
     def draft_length(self) -> int:
         return int(self._lib.sv_adapt_draft_length(ctypes.byref(self._s)))
+
+
+# ---------------------------------------------------------------------------
+# Top-k / top-p filtered verify
+# ---------------------------------------------------------------------------
+def spec_verify_filtered_workspace_size(B: int, R_t: int, V: int) -> int:
+    lib = load()
+    lib.spec_verify_filtered_workspace_size.argtypes = [ctypes.c_int32] * 3
+    lib.spec_verify_filtered_workspace_size.restype = ctypes.c_size_t
+    return int(lib.spec_verify_filtered_workspace_size(int(B), int(R_t), int(V)))
+
+
+def spec_verify_filtered(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor,
+                         cu_draft: torch.Tensor, uniforms: torch.Tensor, temperature: float,
+                         top_k: int = 0, top_p: float = 1.0, mode: Optional[torch.Tensor] = None, *,
+                         out_tokens=None, out_len=None, out_probs=None, want_probs: bool = True,
+                         workspace=None, stream=None):
+    """Verify-and-commit on top-k / top-p filtered distributions.
+    Returns (out_tokens, out_len, out_probs)."""
+    lib = load()
+    fn = lib.spec_verify_filtered
+    P = ctypes.c_void_p
+    fn.argtypes = [P, P, ctypes.c_int, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P, P, P,
+                   ctypes.c_float, ctypes.c_int32, ctypes.c_float, P, P, P, P, ctypes.c_size_t, P]
+    fn.restype = ctypes.c_int
+    B = cu_draft.shape[0] - 1
+    R_t = target.shape[0]
+    V = target.shape[1]
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.full((R_t,), -1, dtype=torch.int32, device=dev)
+    if out_len is None:
+        out_len = torch.zeros(B, dtype=torch.int32, device=dev)
+    if out_probs is None and want_probs:
+        out_probs = torch.empty((R_t, 2), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.zeros(spec_verify_filtered_workspace_size(B, R_t, V), dtype=torch.uint8, device=dev)
+    st = fn(_ptr(target), _ptr(draft), _dtype(target), int(V), int(B), int(R_t), _ptr(draft_tokens),
+            _ptr(cu_draft), _ptr(mode), _ptr(uniforms), float(temperature), int(top_k), float(top_p),
+            _ptr(out_tokens), _ptr(out_len), _ptr(out_probs), _ptr(workspace), workspace.numel(),
+            _stream(stream))
+    _check("spec_verify_filtered", st)
+    return out_tokens, out_len, out_probs

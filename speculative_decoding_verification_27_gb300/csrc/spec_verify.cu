@@ -40,6 +40,7 @@
 
 #include "../../include/spec_verify.h"
 #include "sv_device.cuh"
+#include "sv_filter.cuh"
 
 namespace sv {
 
@@ -129,6 +130,10 @@ constexpr int kStages = SV_STAGES;                  // stages (kStages - 1 in fl
 constexpr int kVPT = SV_VPT;                        // 16-byte vectors per thread per chunk
 constexpr int kChunkBytes = kThreads * 16 * kVPT;   // bytes of one row per stage
 static_assert((kVPT & (kVPT - 1)) == 0, "vectors per thread must be a power of two");
+// Kernel variants: DT & 1 is the logit type (0 fp32, 1 bf16); DT & kFilt
+// marks the top-k / top-p filtered form, in which a logit below its row's
+// threshold counts as -inf everywhere it is read.
+constexpr int kFilt = 2;
 constexpr int kStageBytes = 2 * kChunkBytes;        // target + draft chunk
 constexpr int kRingBytes = kStages * kStageBytes;   // dynamic shared memory per CTA
 constexpr int kPartChunks = SV_PART_CHUNKS;         // ring chunks per draw part
@@ -183,6 +188,8 @@ struct Params {
   DrawDesc* descs;          // [n_slots]
   double* tsum;             // [n_slots, tsum_stride] per-tile sums of r
   double* btile;            // [B, tsum_stride] tile sums of a bonus row's r = S_p p
+  const float* thr;         // [R_t] filter thresholds of the target rows, or NULL
+  const float* thr_d;       // [R_d] filter thresholds of the draft rows, or NULL
   int n_slots, tsum_stride;
   unsigned int* part_done;  // [kMaxTailRows] parts finished per split row
   PartRec* parts;           // [kMaxPartRecs]
@@ -200,6 +207,7 @@ struct Smem {
   int b, t, t0, d0, K, i, greedy, xhat, last, stop, merge, pick, pick2, tok, R_d;
   int zx_ok;        // z_p(x̂) (and z_q(x̂)) were taken from the ring during the row pass
   int btile_ok;     // this bonus row's tile sums were stored during its pass
+  float tau_t, tau_d;  // filter thresholds of the row pair (-inf: unfiltered)
   float zx_p, zx_q, u_acc;
   float redf[kWarps];
   float redf2[kWarps];
@@ -322,12 +330,12 @@ struct SoftAcc {
   // this thread's offset mc after the chunk); the running sums are the same.
   template <int DT, int N>
   __device__ __forceinline__ void add_raw_tiles(const uint4 (&v)[N], float c, float (&tv)[N]) {
-    raise(Raw<DT>::template max_of<N>(v), c);
+    raise(Raw<DT & 1>::template max_of<N>(v), c);
     const f2_t cc = f2_splat(c), nmc = f2_splat(-mc);
 #pragma unroll
     for (int u = 0; u < N; ++u) {
       f2_t z[kPairs], acc = 0ull;
-      Raw<DT>::pairs(v[u], z);
+      Raw<DT & 1>::pairs(v[u], z);
 #pragma unroll
       for (int i = 0; i < kPairs; ++i) {
         const f2_t e = f2_ex2(f2_fma(z[i], cc, nmc));
@@ -342,12 +350,12 @@ struct SoftAcc {
   // N raw vectors at once: one maximum and one rescale check.
   template <int DT, int N>
   __device__ __forceinline__ void add_raw(const uint4 (&v)[N], float c) {
-    raise(Raw<DT>::template max_of<N>(v), c);
+    raise(Raw<DT & 1>::template max_of<N>(v), c);
     const f2_t cc = f2_splat(c), nmc = f2_splat(-mc);
 #pragma unroll
     for (int u = 0; u < N; ++u) {
       f2_t z[kPairs];
-      Raw<DT>::pairs(v[u], z);
+      Raw<DT & 1>::pairs(v[u], z);
       accumulate(z, cc, nmc);
     }
   }
@@ -356,27 +364,65 @@ struct SoftAcc {
 // The kVPT vectors this thread consumes from a ring stage holding elements
 // [x, x + kVPT * kThreads * EPV) of a row: whole vectors inside the row are
 // read, those at or past V read as -inf.
+// Filtered variants: logits below tau become -inf (zero mass).
 template <int DT>
-__device__ __forceinline__ uint4 stage_vector(uint32_t stage, int x, int V, int v, bool whole) {
-  constexpr int EPV = Elem<DT>::kEPV;
-  const int vi = v * kThreads + threadIdx.x;
-  const uint32_t n = Raw<DT>::kNegInf;
-  return (whole || x + vi * EPV < V) ? lds16(stage + 16u * vi) : make_uint4(n, n, n, n);
+__device__ __forceinline__ uint4 mask_below(uint4 v, float tau) {
+  if constexpr ((DT & kFilt) == 0) {
+    return v;
+  } else if constexpr ((DT & 1) == 1) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t lo = __uint_as_float(w[q] << 16) >= tau ? (w[q] & 0xffffu) : 0xff80u;
+      const uint32_t hi = __uint_as_float(w[q] & 0xffff0000u) >= tau ? (w[q] & 0xffff0000u) : 0xff800000u;
+      w[q] = hi | lo;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = __uint_as_float(w[q]) >= tau ? w[q] : 0xff800000u;
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+template <int DT, int N>
+__device__ __forceinline__ void mask_below(float (&f)[N], float tau) {
+  if constexpr ((DT & kFilt) != 0) {
+#pragma unroll
+    for (int j = 0; j < N; ++j)
+      if (!(f[j] >= tau)) f[j] = -INFINITY;
+  }
+}
+template <int DT>
+__device__ __forceinline__ float mask_below(float z, float tau) {
+  if constexpr ((DT & kFilt) != 0) return z >= tau ? z : -INFINITY;
+  return z;
 }
 
 template <int DT>
-__device__ __forceinline__ void stage_vectors(uint32_t stage, int x, int V, uint4 (&rv)[kVPT]) {
-  constexpr int EPV = Elem<DT>::kEPV;
+__device__ __forceinline__ uint4 stage_vector(uint32_t stage, int x, int V, int v, bool whole,
+                                              float tau) {
+  constexpr int EPV = Elem<DT & 1>::kEPV;
+  const int vi = v * kThreads + threadIdx.x;
+  const uint32_t n = Raw<DT & 1>::kNegInf;
+  return (whole || x + vi * EPV < V) ? mask_below<DT>(lds16(stage + 16u * vi), tau)
+                                     : make_uint4(n, n, n, n);
+}
+
+template <int DT>
+__device__ __forceinline__ void stage_vectors(uint32_t stage, int x, int V, uint4 (&rv)[kVPT],
+                                              float tau) {
+  constexpr int EPV = Elem<DT & 1>::kEPV;
   const int tid = threadIdx.x;
   if (x + kVPT * kThreads * EPV <= V) {
 #pragma unroll
-    for (int v = 0; v < kVPT; ++v) rv[v] = lds16(stage + 16u * (v * kThreads + tid));
+    for (int v = 0; v < kVPT; ++v) rv[v] = mask_below<DT>(lds16(stage + 16u * (v * kThreads + tid)), tau);
   } else {
-    const uint32_t n = Raw<DT>::kNegInf;
+    const uint32_t n = Raw<DT & 1>::kNegInf;
 #pragma unroll
     for (int v = 0; v < kVPT; ++v) {
       const int vi = v * kThreads + tid;
-      rv[v] = (x + vi * EPV < V) ? lds16(stage + 16u * vi) : make_uint4(n, n, n, n);
+      rv[v] = (x + vi * EPV < V) ? mask_below<DT>(lds16(stage + 16u * vi), tau) : make_uint4(n, n, n, n);
     }
   }
 }
@@ -406,13 +452,13 @@ __device__ __forceinline__ float warp_tile_totals(float (&ts)[kVPT], int lane, i
 // Element j of vector v of rv (run once per row, by one thread).
 template <int DT>
 __device__ __forceinline__ float pick_element(const uint4 (&rv)[kVPT], int v, int j) {
-  constexpr int EPV = Elem<DT>::kEPV;
+  constexpr int EPV = Elem<DT & 1>::kEPV;
   float out = 0.f;
 #pragma unroll
   for (int u = 0; u < kVPT; ++u) {
     if (u == v) {
       float f[EPV];
-      Elem<DT>::unpack(rv[u], f);
+      Elem<DT & 1>::unpack(rv[u], f);
 #pragma unroll
       for (int q = 0; q < EPV; ++q)
         if (q == j) out = f[q];
@@ -521,16 +567,19 @@ __device__ __forceinline__ bool ring_stream(Smem& s, unsigned char* ring, const 
 // Scalar-load variants for rows that are not 16-byte aligned.
 template <int DT, bool HAS_D>
 __device__ __forceinline__ void stats_pass_scalar(const void* trow, const void* drow, int V, float c,
-                                                  SoftAcc<Elem<DT>::kEPV>& at,
-                                                  SoftAcc<Elem<DT>::kEPV>& ad) {
-  constexpr int EPV = Elem<DT>::kEPV;
+                                                  SoftAcc<Elem<DT & 1>::kEPV>& at,
+                                                  SoftAcc<Elem<DT & 1>::kEPV>& ad, float tau_t,
+                                                  float tau_d) {
+  constexpr int EPV = Elem<DT & 1>::kEPV;
   constexpr int TILE = kThreads * EPV;
   for (int x = threadIdx.x * EPV; x < V; x += TILE) {
     float f[EPV];
-    load_chunk<DT, false>(trow, x, V, f);
+    load_chunk<DT & 1, false>(trow, x, V, f);
+    mask_below<DT>(f, tau_t);
     at.add(f, c);
     if constexpr (HAS_D) {
-      load_chunk<DT, false>(drow, x, V, f);
+      load_chunk<DT & 1, false>(drow, x, V, f);
+      mask_below<DT>(f, tau_d);
       ad.add(f, c);
     }
   }
@@ -538,11 +587,11 @@ __device__ __forceinline__ void stats_pass_scalar(const void* trow, const void* 
 
 template <int DT>
 __device__ __forceinline__ void argmax_scalar(const void* trow, int V, float& bv, int& bi) {
-  constexpr int EPV = Elem<DT>::kEPV;
+  constexpr int EPV = Elem<DT & 1>::kEPV;
   constexpr int TILE = kThreads * EPV;
   for (int x = threadIdx.x * EPV; x < V; x += TILE) {
     float f[EPV];
-    load_chunk<DT, false>(trow, x, V, f);
+    load_chunk<DT & 1, false>(trow, x, V, f);
 #pragma unroll
     for (int j = 0; j < EPV; ++j)
       if (f[j] > bv) {
@@ -650,6 +699,7 @@ struct DrawArgs {
   float mcp, mcq;
   float bhi, blo;    // beta = S_p / S_q as a double-float pair
   double u2;
+  float tau_p, tau_q;  // filter thresholds of the two rows (-inf: unfiltered)
 };
 
 __device__ __forceinline__ DrawArgs make_draw_args(const Params& P, size_t rowb, int row, int drow,
@@ -667,6 +717,8 @@ __device__ __forceinline__ DrawArgs make_draw_args(const Params& P, size_t rowb,
   a.bhi = (float)beta;
   a.blo = (float)(beta - (double)a.bhi);
   a.u2 = (double)__ldg(&P.uniforms[2 * (size_t)row + 1]);
+  a.tau_p = P.thr ? __ldg(&P.thr[row]) : -INFINITY;
+  a.tau_q = (P.thr_d && kind == kResidual) ? __ldg(&P.thr_d[drow]) : -INFINITY;
   return a;
 }
 
@@ -696,7 +748,7 @@ __device__ __forceinline__ void residual_of(const DrawArgs& a, float c, const fl
 template <int DT, bool VEC>
 __device__ bool tile_sums(const Params& P, Smem& s, unsigned char* ring, const DrawArgs& a,
                           int tile0, int ntl) {
-  constexpr int EPV = Elem<DT>::kEPV;
+  constexpr int EPV = Elem<DT & 1>::kEPV;
   constexpr int TILE = kThreads * EPV;
   const int V = P.V;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -712,9 +764,9 @@ __device__ bool tile_sums(const Params& P, Smem& s, unsigned char* ring, const D
   };
   if constexpr (VEC) {
     // Tiles of a chunk are kVPT consecutive tiles; tile0 is chunk aligned.
-    const size_t off = (size_t)tile0 * TILE * Elem<DT>::kBytes;
-    const size_t row_bytes = (size_t)V * Elem<DT>::kBytes;
-    size_t len = (size_t)ntl * TILE * Elem<DT>::kBytes;
+    const size_t off = (size_t)tile0 * TILE * Elem<DT & 1>::kBytes;
+    const size_t row_bytes = (size_t)V * Elem<DT & 1>::kBytes;
+    size_t len = (size_t)ntl * TILE * Elem<DT & 1>::kBytes;
     if (off + len > row_bytes) len = row_bytes - off;
     const bool res = a.kind == kResidual;
     const bool onehot = a.kind == kOneHot;
@@ -731,10 +783,10 @@ __device__ bool tile_sums(const Params& P, Smem& s, unsigned char* ring, const D
 #pragma unroll
       for (int v = 0; v < kVPT; ++v) {
         f2_t zp[NP], acc = 0ull;
-        Raw<DT>::pairs(stage_vector<DT>(stage, xc, V, v, whole), zp);
+        Raw<DT & 1>::pairs(stage_vector<DT>(stage, xc, V, v, whole, a.tau_p), zp);
         if (res) {
           f2_t zq[NP];
-          Raw<DT>::pairs(stage_vector<DT>(stage + kChunkBytes, xc, V, v, whole), zq);
+          Raw<DT & 1>::pairs(stage_vector<DT>(stage + kChunkBytes, xc, V, v, whole, a.tau_q), zq);
 #pragma unroll
           for (int i = 0; i < NP; ++i) {
             const f2_t ep = f2_ex2(f2_fma(zp[i], cc, nmcp));
@@ -770,8 +822,12 @@ __device__ bool tile_sums(const Params& P, Smem& s, unsigned char* ring, const D
     for (int l = 0; l < ntl; ++l) {
       const int x = (tile0 + l) * TILE + tid * EPV;
       float zp[EPV], zq[EPV];
-      load_chunk<DT, false>(a.trow, x, V, zp);
-      if (a.kind == kResidual) load_chunk<DT, false>(a.drow, x, V, zq);
+      load_chunk<DT & 1, false>(a.trow, x, V, zp);
+      mask_below<DT>(zp, a.tau_p);
+      if (a.kind == kResidual) {
+        load_chunk<DT & 1, false>(a.drow, x, V, zq);
+        mask_below<DT>(zq, a.tau_q);
+      }
       one_tile(l, zp, zq);
     }
     __syncthreads();
@@ -787,7 +843,7 @@ __device__ bool tile_sums(const Params& P, Smem& s, unsigned char* ring, const D
 // sum exceeds u' * Z.
 template <int DT, bool VEC>
 __device__ int locate_token(const Params& P, Smem& s, const DrawArgs& a, double tt, int ntiles) {
-  constexpr int EPV = Elem<DT>::kEPV;
+  constexpr int EPV = Elem<DT & 1>::kEPV;
   constexpr int TILE = kThreads * EPV;
   const int V = P.V;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -819,8 +875,12 @@ __device__ int locate_token(const Params& P, Smem& s, const DrawArgs& a, double 
   // The chosen tile: thread k spans [wexcl[w] + lane_lo, wexcl[w] + incl).
   const int x = kt * TILE + tid * EPV;
   float zp[EPV], zq[EPV], r[EPV];
-  load_chunk<DT, VEC>(a.trow, x, V, zp);
-  if (a.kind == kResidual) load_chunk<DT, VEC>(a.drow, x, V, zq);
+  load_chunk<DT & 1, VEC>(a.trow, x, V, zp);
+  mask_below<DT>(zp, a.tau_p);
+  if (a.kind == kResidual) {
+    load_chunk<DT & 1, VEC>(a.drow, x, V, zq);
+    mask_below<DT>(zq, a.tau_q);
+  }
   residual_of<EPV>(a, P.c, zp, zq, x, r);
   float ts = 0.f;
 #pragma unroll
@@ -862,7 +922,7 @@ __device__ int locate_token(const Params& P, Smem& s, const DrawArgs& a, double 
 // copy timeout.
 template <int DT, bool VEC>
 __device__ int draw_whole(const Params& P, Smem& s, unsigned char* ring, const DrawArgs& a) {
-  constexpr int TILE = kThreads * Elem<DT>::kEPV;
+  constexpr int TILE = kThreads * Elem<DT & 1>::kEPV;
   const int ntiles = (P.V + TILE - 1) / TILE;
   if (!tile_sums<DT, VEC>(P, s, ring, a, 0, ntiles)) return -2;
   double tt = 0.0;
@@ -876,10 +936,10 @@ template <int DT>
 __device__ void finish_draw(const Params& P, const DrawArgs& a, double Sp, double Sq, int y,
                             int bonus_row) {
   float qy;
-  const float zp = Elem<DT>::scalar(a.trow, y);
+  const float zp = mask_below<DT>(Elem<DT & 1>::scalar(a.trow, y), a.tau_p);
   const float py = (float)((double)exp2f(fmaf(zp, P.c, -a.mcp)) / Sp);
   if (a.kind == kResidual) {
-    const float zq = Elem<DT>::scalar(a.drow, y);
+    const float zq = mask_below<DT>(Elem<DT & 1>::scalar(a.drow, y), a.tau_q);
     qy = (float)((double)exp2f(fmaf(zq, P.c, -a.mcq)) / Sq);
   } else if (a.kind == kOneHot) {
     qy = (y == a.xhat) ? 1.f : 0.f;
@@ -931,12 +991,12 @@ __device__ bool claim_draw_part(const Params& P, int& slot_out, int& part_out) {
 template <int DT, bool VEC>
 __device__ __noinline__ bool draw_part(const Params& P, Smem& s, unsigned char* ring, int slot,
                                        int part) {
-  constexpr int TILE = kThreads * Elem<DT>::kEPV;
+  constexpr int TILE = kThreads * Elem<DT & 1>::kEPV;
   const int tid = threadIdx.x;
   const DrawDesc* d = &P.descs[slot];
   const double Sp = __ldcg(&d->Sp), Sq = __ldcg(&d->Sq);
   const int kind = __ldcg(&d->kind);
-  const DrawArgs a = make_draw_args(P, (size_t)P.V * Elem<DT>::kBytes, __ldcg(&d->row),
+  const DrawArgs a = make_draw_args(P, (size_t)P.V * Elem<DT & 1>::kBytes, __ldcg(&d->row),
                                     __ldcg(&d->drow), kind, __ldcg(&d->xhat), __ldcg(&d->mcp),
                                     __ldcg(&d->mcq), Sp, Sq);
   const int nparts = __ldcg(&d->nparts);
@@ -982,7 +1042,7 @@ __device__ __noinline__ bool draw_part(const Params& P, Smem& s, unsigned char* 
     if (tid == 0) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
     y = 0;
   }
-  if (tid == 0) finish_draw<DT>(P, used, Sp, Sq, y, __ldcg(&d->bonus_row));
+  if (tid == 0) finish_draw<DT>(P, a, Sp, Sq, y, __ldcg(&d->bonus_row));
   return true;
 }
 
@@ -1025,9 +1085,9 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
   if (VEC && kind == kBonus && (__ldcg(&P.rows[srow].accept) & 2u)) {
     // The bonus row left its tile sums: only the chosen tile is read again.
     if (tid == 0) atomicAdd(&P.ws->committed, 1u);
-    const DrawArgs a = make_draw_args(P, (size_t)P.V * Elem<DT>::kBytes, srow, drow, kind, xhat,
+    const DrawArgs a = make_draw_args(P, (size_t)P.V * Elem<DT & 1>::kBytes, srow, drow, kind, xhat,
                                       mcp, mcq, Sp, Sq);
-    constexpr int TILE = kThreads * Elem<DT>::kEPV;
+    constexpr int TILE = kThreads * Elem<DT & 1>::kEPV;
     const int ntiles = (P.V + TILE - 1) / TILE;
     const double tt = tid < ntiles ? __ldcg(&P.btile[(size_t)b * P.tsum_stride + tid]) : 0.0;
     int y = locate_token<DT, VEC>(P, s, a, tt, ntiles);
@@ -1043,7 +1103,7 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
   // The request counts as committed only once its draw is published (or
   // kept whole here), so that idle CTAs linger until they can take parts.
   if (tid == 0) {
-    constexpr int TILE = kThreads * Elem<DT>::kEPV;
+    constexpr int TILE = kThreads * Elem<DT & 1>::kEPV;
     const int nchunks = ((P.V + TILE - 1) / TILE + kVPT - 1) / kVPT;
     // When every request's draw, cut into single chunks, fits in one wave of
     // CTAs (a small batch), use single-chunk parts; otherwise larger ones.
@@ -1052,7 +1112,7 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
     nparts = nparts > kMaxParts ? kMaxParts : nparts;
     // Parts carry a fixed cost (descriptor, ring start, a global merge); a
     // draw that streams less than kMinPublishBytes is faster kept whole.
-    const size_t draw_bytes = (size_t)P.V * Elem<DT>::kBytes * (kind == kResidual ? 2 : 1);
+    const size_t draw_bytes = (size_t)P.V * Elem<DT & 1>::kBytes * (kind == kResidual ? 2 : 1);
     s.slot = -1;
     if (nparts > 1 && draw_bytes >= kMinPublishBytes &&
         ld_relaxed_gpu(&P.ws->next_item) + kPublishPct * gridDim.x / 100u >= s.n_items) {
@@ -1090,7 +1150,7 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
     }
     return true;
   }
-  const DrawArgs a = make_draw_args(P, (size_t)P.V * Elem<DT>::kBytes, srow, drow, kind, xhat, mcp,
+  const DrawArgs a = make_draw_args(P, (size_t)P.V * Elem<DT & 1>::kBytes, srow, drow, kind, xhat, mcp,
                                     mcq, Sp, Sq);
   int y = draw_whole<DT, VEC>(P, s, ring, a);
   if (y == -2) return false;
@@ -1108,7 +1168,7 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
     if (tid == 0) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
     y = 0;
   }
-  if (tid == 0) finish_draw<DT>(P, used, Sp, Sq, y, t0 + K);
+  if (tid == 0) finish_draw<DT>(P, a, Sp, Sq, y, t0 + K);
   return true;
 }
 
@@ -1186,6 +1246,8 @@ __device__ __noinline__ void row_meta(const Params& P, Smem& s, int o) {
   }
   s.u_acc = u;
   s.zx_ok = 0;
+  s.tau_t = P.thr ? __ldg(&P.thr[t]) : -INFINITY;
+  s.tau_d = (P.thr_d && i < K) ? __ldg(&P.thr_d[d0 + i]) : -INFINITY;
   s.btile_ok = 0;
   s.b = b;
   s.t = t;
@@ -1204,11 +1266,11 @@ template <int DT, bool VEC>
 __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const char* trow,
                             const char* drow, bool greedy, int c0, int c1, PartRec& st,
                             bool btiles, int b) {
-  constexpr int EPV = Elem<DT>::kEPV;
-  constexpr int CH = kChunkBytes / Elem<DT>::kBytes;
+  constexpr int EPV = Elem<DT & 1>::kEPV;
+  constexpr int CH = kChunkBytes / Elem<DT & 1>::kBytes;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int V = P.V;
-  const size_t rowb = (size_t)V * Elem<DT>::kBytes;
+  const size_t rowb = (size_t)V * Elem<DT & 1>::kBytes;
   const size_t off = (size_t)c0 * kChunkBytes;
   const size_t end = (size_t)c1 * kChunkBytes < rowb ? (size_t)c1 * kChunkBytes : rowb;
   const size_t len = end > off ? end - off : 0;
@@ -1220,8 +1282,8 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
     if constexpr (VEC) {
       ok = ring_stream(s, ring, trow + off, nullptr, len, false, [&](int k, uint32_t stage) {
         uint4 rv[kVPT];
-        stage_vectors<DT>(stage, x0 + k * CH, V, rv);
-        const float cm = Raw<DT>::template max_of<kVPT>(rv);
+        stage_vectors<DT>(stage, x0 + k * CH, V, rv, s.tau_t);
+        const float cm = Raw<DT & 1>::template max_of<kVPT>(rv);
         if (cm > bv) {
           // A new maximum: its first occurrence in this thread's elements,
           // which it visits in increasing index order.
@@ -1229,7 +1291,7 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
 #pragma unroll
           for (int v = kVPT - 1; v >= 0; --v) {
             float f[EPV];
-            Elem<DT>::unpack(rv[v], f);
+            Elem<DT & 1>::unpack(rv[v], f);
 #pragma unroll
             for (int j = EPV - 1; j >= 0; --j)
               if (f[j] == cm) first = x0 + k * CH + (v * kThreads + tid) * EPV + j;
@@ -1268,7 +1330,7 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
       // for the accept test, so that test needs no global load.
       const int xh = s.xhat;
       int kx = -1, vx = 0, jx = 0;
-      if (xh >= x0 && (size_t)(xh - x0) < len / Elem<DT>::kBytes) {
+      if (xh >= x0 && (size_t)(xh - x0) < len / Elem<DT & 1>::kBytes) {
         const int e = xh - x0;
         kx = e / CH;
         const int vi = (e - kx * CH) / EPV;
@@ -1286,7 +1348,7 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
         // Bonus rows stream alone (no draft row, no proposed token).
         ok = ring_stream(s, ring, trow + off, nullptr, len, false, [&](int k, uint32_t stage) {
           uint4 rv[kVPT];
-          stage_vectors<DT>(stage, x0 + k * CH, V, rv);
+          stage_vectors<DT>(stage, x0 + k * CH, V, rv, s.tau_t);
           float tv[kVPT];
           at.template add_raw_tiles<DT, kVPT>(rv, P.c, tv);
           const bool live = at.m != -INFINITY;
@@ -1304,14 +1366,14 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
         ok = ring_stream(s, ring, trow + off, has_d ? drow + off : nullptr, len, false,
                          [&](int k, uint32_t stage) {
           uint4 rv[kVPT];
-          stage_vectors<DT>(stage, x0 + k * CH, V, rv);
+          stage_vectors<DT>(stage, x0 + k * CH, V, rv, s.tau_t);
           if (k == kx) {
             s.zx_p = pick_element<DT>(rv, vx, jx);
             s.zx_ok = 1;
           }
           at.template add_raw<DT, kVPT>(rv, P.c);
           if (has_d) {
-            stage_vectors<DT>(stage + kChunkBytes, x0 + k * CH, V, rv);
+            stage_vectors<DT>(stage + kChunkBytes, x0 + k * CH, V, rv, s.tau_d);
             if (k == kx) s.zx_q = pick_element<DT>(rv, vx, jx);
             ad.template add_raw<DT, kVPT>(rv, P.c);
           }
@@ -1319,9 +1381,9 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
       }
     } else {
       if (has_d)
-        stats_pass_scalar<DT, true>(trow, drow, V, P.c, at, ad);
+        stats_pass_scalar<DT, true>(trow, drow, V, P.c, at, ad, s.tau_t, s.tau_d);
       else
-        stats_pass_scalar<DT, false>(trow, drow, V, P.c, at, ad);
+        stats_pass_scalar<DT, false>(trow, drow, V, P.c, at, ad, s.tau_t, s.tau_d);
     }
     float mcp, mcq;
     double Sp, Sq;
@@ -1400,7 +1462,7 @@ template <int DT>
 __device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const PartRec& st) {
   const int b = s.b, d0 = s.d0, K = s.K, i = s.i, xhat = s.xhat;
   const bool greedy = s.greedy != 0;
-  const size_t rowb = (size_t)P.V * Elem<DT>::kBytes;
+  const size_t rowb = (size_t)P.V * Elem<DT & 1>::kBytes;
   const char* trow = static_cast<const char*>(P.target) + (size_t)t * rowb;
   const bool has_d = !greedy && i < K && P.draft != nullptr;
   const char* drow = has_d ? static_cast<const char*>(P.draft) + (size_t)(d0 + i) * rowb : nullptr;
@@ -1431,13 +1493,13 @@ __device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const P
       if (xhat >= 0) {
         // p(x̂) = 2^(z c - mc_p) / S_p, and min(1, p/q) with q from the
         // draft row or q = 1 for a one-hot proposal.
-        const float zp = s.zx_ok ? s.zx_p : Elem<DT>::scalar(trow, xhat);
+        const float zp = s.zx_ok ? s.zx_p : mask_below<DT>(Elem<DT & 1>::scalar(trow, xhat), s.tau_t);
         const float ap = fmaf(zp, P.c, -mcp);
         const double pd = (double)exp2f(ap) / Sp;
         double rho;
         double qd = 1.0;
         if (has_d) {
-          const float zq = s.zx_ok ? s.zx_q : Elem<DT>::scalar(drow, xhat);
+          const float zq = s.zx_ok ? s.zx_q : mask_below<DT>(Elem<DT & 1>::scalar(drow, xhat), s.tau_d);
           const float aq = fmaf(zq, P.c, -mcq);
           qd = (double)exp2f(aq) / Sq;
           rho = (zq == -INFINITY) ? 0.0 : fmin(1.0, (double)exp2f(ap - aq) * (Sq / Sp));
@@ -1499,7 +1561,7 @@ __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int 
   __syncthreads();
   const int b = s.b, t = s.t, t0 = s.t0, d0 = s.d0, K = s.K, i = s.i;
   const bool greedy = s.greedy != 0;
-  const size_t rowb = (size_t)P.V * Elem<DT>::kBytes;
+  const size_t rowb = (size_t)P.V * Elem<DT & 1>::kBytes;
   const char* trow = static_cast<const char*>(P.target) + (size_t)t * rowb;
   const bool has_d = !greedy && i < K && P.draft != nullptr;
   const char* drow = has_d ? static_cast<const char*>(P.draft) + (size_t)(d0 + i) * rowb : nullptr;
@@ -1575,7 +1637,7 @@ __global__ void __launch_bounds__(kThreads, SV_MINBLOCKS) verify_kernel(Params P
       W = min(R_t, min(kTailWaves * gridDim.x, kMaxTailRows));
       np = kRowParts;
       if (R_t < gridDim.x) np = max(np, gridDim.x / R_t);  // few rows: spread each row out
-      const unsigned nch = (unsigned)(((size_t)P.V * Elem<DT>::kBytes + kChunkBytes - 1) / kChunkBytes);
+      const unsigned nch = (unsigned)(((size_t)P.V * Elem<DT & 1>::kBytes + kChunkBytes - 1) / kChunkBytes);
       np = min(np, min(kMaxRowParts, nch));
       if (W > 0) np = min(np, kMaxPartRecs / W);
       if (np < 2) W = 0, np = 1;
@@ -1693,7 +1755,7 @@ static size_t ws_size(long long B, long long R_t, int V) {
 // Resident CTAs per device for each kernel variant, filled on first use
 // (which also raises the variant's dynamic shared-memory limit).
 constexpr int kMaxDevices = 64;
-static std::atomic<int> g_resident[kMaxDevices][2][2];
+static std::atomic<int> g_resident[kMaxDevices][4][2];
 
 template <bool VEC>
 static constexpr int dyn_smem() { return VEC ? kRingBytes : 0; }
@@ -1740,7 +1802,8 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
                             const uint8_t* mode, const float* uniforms, float temperature,
                             int32_t* out_tokens, int32_t* out_len, float* out_probs,
                             void* workspace, size_t workspace_bytes, void* stream,
-                            int greedy_all) {
+                            int greedy_all, const float* thr = nullptr,
+                            const float* thr_d = nullptr) {
   if (dtype != SV_FP32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
   if (B < 0 || V < 1 || V > max_vocab(dtype)) return SV_ERR_INVALID_ARG;
   if (B == 0) return SV_OK;
@@ -1785,16 +1848,24 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
   P.rows = reinterpret_cast<RowRec*>(ws + L.rows);
   P.row_cap = (long long)((workspace_bytes - L.rows) / sizeof(RowRec));
   P.greedy_all = greedy_all;
+  P.thr = thr;
+  P.thr_d = thr_d;
 
   // Bulk copies need 16-byte aligned row starts and 16-byte multiples.
   const bool vec = ((uintptr_t)target % 16 == 0) && (!P.draft || (uintptr_t)P.draft % 16 == 0) &&
                    (((size_t)V * es) % 16 == 0);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (dtype == SV_BF16)
+  if (thr) {
+    if (dtype == SV_BF16)
+      e = vec ? launch<1 | kFilt, true>(P, st) : launch<1 | kFilt, false>(P, st);
+    else
+      e = vec ? launch<0 | kFilt, true>(P, st) : launch<0 | kFilt, false>(P, st);
+  } else if (dtype == SV_BF16) {
     e = vec ? launch<1, true>(P, st) : launch<1, false>(P, st);
-  else
+  } else {
     e = vec ? launch<0, true>(P, st) : launch<0, false>(P, st);
+  }
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -1851,6 +1922,64 @@ sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logit
                                     cudaMemcpyDeviceToDevice, st) != cudaSuccess)
     return SV_ERR_CUDA;
   return SV_OK;
+}
+
+// Filtered form: the per-row thresholds come first in the workspace, then
+// the verify kernel's own workspace.
+static size_t filter_bytes(int64_t R_t, int64_t B) {
+  return sv::align16((size_t)R_t * 4) + sv::align16((size_t)(R_t - B) * 4 + 4);
+}
+
+size_t spec_verify_filtered_workspace_size(int32_t B, int32_t R_t, int32_t V) {
+  if (B < 0 || R_t < B || V < 1) return 0;
+  return filter_bytes(R_t, B) + sv::ws_size(B, R_t > 0 ? R_t : 1, V);
+}
+
+sv_status spec_verify_filtered(const void* target_logits, const void* draft_logits,
+                               sv_dtype dtype, int32_t V, int32_t B, int32_t R_t,
+                               const int32_t* draft_tokens, const int32_t* cu_draft,
+                               const uint8_t* mode, const float* uniforms, float temperature,
+                               int32_t top_k, float top_p, int32_t* out_tokens,
+                               int32_t* out_len, float* out_probs, void* workspace,
+                               size_t workspace_bytes, void* cuda_stream) {
+  if (B < 0 || R_t < B || top_k < 0 || !(top_p > 0.f) || top_p != top_p) return SV_ERR_INVALID_ARG;
+  if (dtype != SV_FP32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!workspace || (uintptr_t)workspace % 16 || !cu_draft || !target_logits) return SV_ERR_INVALID_ARG;
+  const size_t fb = filter_bytes(R_t, B);
+  if (workspace_bytes < fb) return SV_ERR_INVALID_ARG;
+  const bool use_k = top_k >= 1 && top_k < V, use_p = top_p < 1.f;
+  char* ws = static_cast<char*>(workspace);
+  if (!use_k && !use_p)  // nothing to filter: the plain step
+    return sv::run_verify(target_logits, draft_logits, dtype, V, B, draft_tokens, cu_draft, mode,
+                          uniforms, temperature, out_tokens, out_len, out_probs, ws + fb,
+                          workspace_bytes - fb, cuda_stream, 0);
+  if (!(temperature > 0.f) || !std::isfinite(temperature) || V < 1 || V > sv::max_vocab(dtype))
+    return SV_ERR_INVALID_ARG;
+  const size_t es = dtype == SV_FP32 ? 4 : 2;
+  if ((uintptr_t)target_logits % es || (draft_logits && (uintptr_t)draft_logits % es))
+    return SV_ERR_INVALID_ARG;
+  sv::FtParams fp;
+  fp.target = target_logits;
+  fp.draft = draft_logits;
+  fp.V = V;
+  fp.B = B;
+  fp.rows_t = R_t;
+  fp.cu = cu_draft;
+  fp.mode = mode;
+  fp.c = (float)(1.4426950408889634 / (double)temperature);
+  fp.top_k = use_k ? top_k : 0;
+  fp.top_p = use_p ? top_p : 1.f;
+  fp.vec = ((uintptr_t)target_logits % 16 == 0) && (!draft_logits || (uintptr_t)draft_logits % 16 == 0) &&
+           (((size_t)V * es) % 16 == 0);
+  fp.thr_t = reinterpret_cast<float*>(ws);
+  fp.thr_d = reinterpret_cast<float*>(ws + sv::align16((size_t)R_t * 4));
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (sv::launch_thresholds(fp, dtype, st) != cudaSuccess) return SV_ERR_CUDA;
+  return sv::run_verify(target_logits, draft_logits, dtype, V, B, draft_tokens, cu_draft, mode,
+                        uniforms, temperature, out_tokens, out_len, out_probs, ws + fb,
+                        workspace_bytes - fb, cuda_stream, 0, fp.thr_t,
+                        draft_logits ? fp.thr_d : nullptr);
 }
 
 size_t spec_verify_workspace_size(int32_t B, int32_t R_t, int32_t V) {

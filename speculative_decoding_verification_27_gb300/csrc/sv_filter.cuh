@@ -1,0 +1,27 @@
+// sv_filter.cuh -- launcher of the per-row top-k / top-p threshold kernel
+// (filter.cu), used by the filtered verify entry point.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sv {
+
+struct FtParams {
+  const void* target;   // [R_t, V]
+  const void* draft;    // [R_d, V] or NULL (one-hot proposals: no draft rows)
+  int V, B;
+  int rows_t;           // target rows the caller holds (threshold writes stop there)
+  const int32_t* cu;    // [B+1]
+  const uint8_t* mode;  // [B] or NULL
+  float c;              // log2(e) / T
+  int top_k;            // 0: off
+  float top_p;          // >= 1: off
+  bool vec;             // rows are 16-byte aligned with V * s % 16 == 0
+  float* thr_t;         // [rows_t]
+  float* thr_d;         // [rows_t - B]
+};
+
+cudaError_t launch_thresholds(const FtParams& P, int dtype, cudaStream_t st);
+
+}  // namespace sv

@@ -1,0 +1,90 @@
+"""GPU parity of spec_verify_filtered (top-k / top-p on target and draft rows)
+against the float64 oracle's filtered verify, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import parity
+from speculative_decoding_verification_27_gb300 import api
+from speculative_decoding_verification_27_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(batch, top_k, top_p):
+    import oracle
+    db = parity.to_device(batch)
+    tok, ln, pr = api.spec_verify_filtered(db.target, db.draft, db.draft_tokens, db.cu_draft, db.uniforms,
+                                           db.temperature, top_k, top_p, db.mode)
+    torch.cuda.synchronize()
+    ora = oracle.spec_verify(batch.target, batch.draft, batch.draft_tokens, batch.cu_draft, batch.uniforms,
+                             batch.temperature, batch.mode, top_k=top_k, top_p=top_p)
+    return parity.compare(batch, (tok.cpu().numpy(), ln.cpu().numpy(), pr.cpu().numpy()), ora)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("V", [33, 1000, 4097, 8200])
+@pytest.mark.parametrize("top_k,top_p", [(5, 1.0), (0, 0.8), (20, 0.9), (1, 1.0), (0, 0.3)])
+def test_filtered_small_vocab(cuda_lib, dtype, V, top_k, top_p):
+    Ks = np.array([0, 1, 3, 5, 2, 0, 4, 6], np.int32)
+    b = W.gaussian_sampling(seed=500 + V + top_k, B=Ks.size, K=Ks, V=V, sigma=2.0, draft_sigma=0.7,
+                            T=0.9, dtype=dtype)
+    b.mode = np.array([0, 1, 0, 0, 1, 0, 0, 0], np.uint8)
+    rep = _run(b, top_k, top_p)
+    assert rep.mismatched_requests <= 1
+
+
+@pytest.mark.parametrize("top_k,top_p", [(50, 0.9), (0, 0.95), (1000, 1.0)])
+def test_filtered_large_vocab_peaked_rows(cuda_lib, top_k, top_p):
+    """Rows of the benchmark's shape (V=151936 bf16, T=0.7, peaked rank
+    scores), 24 requests."""
+    b = W.config3(seed=510 + top_k, B=24)
+    rep = _run(b, top_k, top_p)
+    print(rep.as_dict())
+    assert rep.mismatched_requests <= 1
+
+
+def test_filtered_one_hot_and_ties(cuda_lib):
+    """One-hot proposals filter the target only; logits on a coarse grid make
+    long tie groups at every threshold."""
+    rng = np.random.default_rng(520)
+    b = W.gaussian_sampling(seed=521, B=40, K=4, V=3000, sigma=1.0, draft_sigma=0.5, T=1.0)
+    b.draft = None
+    rep = _run(b, 40, 0.85)
+    assert rep.mismatched_requests <= 1
+    b = W.gaussian_sampling(seed=522, B=40, K=4, V=2048, sigma=2.0, draft_sigma=1.0, T=1.0)
+    b.target = (np.round(b.target * 2) / 2).astype(np.float32)   # values on a 0.5 grid
+    b.draft = (np.round(b.draft * 2) / 2).astype(np.float32)
+    for k, p in [(7, 1.0), (0, 0.6), (30, 0.75)]:
+        rep = _run(b, k, p)
+        assert rep.mismatched_requests <= 1
+
+
+def test_filters_off_equal_the_plain_step(cuda_lib):
+    b = W.config5(seed=530, B=48, V=20000)
+    db = parity.to_device(b)
+    a = api.spec_verify(db.target, db.draft, db.draft_tokens, db.cu_draft, db.uniforms, db.temperature, db.mode)
+    f = api.spec_verify_filtered(db.target, db.draft, db.draft_tokens, db.cu_draft, db.uniforms,
+                                 db.temperature, 0, 1.0, db.mode)
+    torch.cuda.synchronize()
+    assert torch.equal(a[1], f[1]) and torch.equal(a[2], f[2])
+    t0 = b.cu_draft[:-1] + np.arange(b.B)
+    ta, tf, ln = a[0].cpu().numpy(), f[0].cpu().numpy(), a[1].cpu().numpy()
+    for i in range(b.B):
+        assert np.array_equal(ta[t0[i]:t0[i] + ln[i]], tf[t0[i]:t0[i] + ln[i]])
+
+
+def test_filtered_bad_offsets_stay_in_bounds(cuda_lib):
+    """Offsets that claim more rows than the caller holds: the thresholds
+    stop at the caller's rows and the step reports the offsets."""
+    b = W.gaussian_sampling(seed=540, B=6, K=3, V=512, sigma=1.0, draft_sigma=0.5, T=1.0)
+    db = parity.to_device(b)
+    cu_bad = db.cu_draft.clone()
+    cu_bad[-1] += 50
+    ws = torch.zeros(api.spec_verify_filtered_workspace_size(b.B, b.R_t, b.V), dtype=torch.uint8,
+                     device="cuda")
+    api.spec_verify_filtered(db.target, db.draft, db.draft_tokens, cu_bad, db.uniforms, 1.0, 10, 0.9,
+                             workspace=ws)
+    torch.cuda.synchronize()
+    fb = api.spec_verify_filtered_workspace_size(b.B, b.R_t, b.V) - api.spec_verify_workspace_size(b.B, b.R_t, b.V)
+    assert api.sv_check_status(ws[fb:]) & api.SV_DATA_BAD_OFFSETS
