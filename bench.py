@@ -389,6 +389,8 @@ EXTRA_WORKLOADS = {
                     "counter block",
     "topkp_b256": "top-k 50 / top-p 0.9 filtered sampling verify on the benchmark batch (B=256 K=7 "
                   "V=151936 bf16 T=0.7, peaked rank-score rows)",
+    "candidates_b64x4": "64 requests x 4 draft candidates of 5 tokens (V=32000 bf16, T=1.0), verified as "
+                        "256 requests, then the longest commit kept per request",
 }
 FILTER_K, FILTER_P = 50, 0.9
 
@@ -475,6 +477,9 @@ def _extra_setup(name, seed):
         batches = [W.config5(seed=seed)]
     elif name == "topkp_b256":
         batches = [W.config3(seed=seed)]
+    elif name == "candidates_b64x4":
+        batches = [W.gaussian_sampling(seed=seed, B=256, K=5, V=32000, sigma=2.0, draft_sigma=0.5, T=1.0,
+                                       dtype="bf16")]
     else:
         raise SystemExit(f"unknown workload {name}")
     dbs = [parity.to_device(b) for b in batches]
@@ -487,6 +492,11 @@ def _extra_setup(name, seed):
     k = [0]
     greedy_only = name == "greedy_b64"
     filtered = name == "topkp_b256"
+    cands = name == "candidates_b64x4"
+    if cands:
+        cu_cand = torch.arange(0, 257, 4, dtype=torch.int32, device="cuda")
+        best = torch.empty(64, dtype=torch.int32, device="cuda")
+        best_len = torch.empty(64, dtype=torch.int32, device="cuda")
     if filtered:
         ws = torch.zeros(api.spec_verify_filtered_workspace_size(b0.B, b0.R_t, b0.V), dtype=torch.uint8,
                          device="cuda")
@@ -505,6 +515,8 @@ def _extra_setup(name, seed):
             api.spec_verify(db.target, db.draft, db.draft_tokens, db.cu_draft, db.uniforms,
                             db.temperature, db.mode, out_tokens=ot, out_len=ol, out_probs=op,
                             workspace=ws)
+            if cands:
+                api.sv_select_candidates(cu_cand, ol, best=best, best_len=best_len)
 
     d0 = dbs[0]
     host = {f: (getattr(d0, f), getattr(d0, f).cpu().pin_memory())
@@ -539,7 +551,8 @@ def _extra_setup(name, seed):
             "temperature": b0.temperature, "input_sets": len(batches)}
     if filtered:
         desc.update({"top_k": FILTER_K, "top_p": FILTER_P})
-    return desc, host, [ot, ol], step, units, "rows/s", nbytes, name not in ("ragged_b512", "topkp_b256"), \
+    outs = [ot, ol] if not cands else [ot, ol, best, best_len]
+    return desc, host, outs, step, units, "rows/s", nbytes, name not in ("ragged_b512", "topkp_b256"), \
         oracle_fn, check
 
 
@@ -628,8 +641,9 @@ def run_extra(args):
                                                             "onehot_b128", "metrics_b512")
                                    else spot["rows"]) / dt,
                          "unit": unit, "cores": threads, "kind": "oracle",
-                         "sample": {"ragged_b512": "64 of 512 requests",
-                                    "topkp_b256": "64 of 256 requests"}.get(args.workload, "the whole step")},
+                         "sample": {"ragged_b512": "64 of 512 requests", "topkp_b256": "64 of 256 requests",
+                                    "candidates_b64x4": "64 of 256 candidates (verify only)"}.get(
+                                        args.workload, "the whole step")},
         "parity_spot_check": spot,
     }
     print(json.dumps(line))

@@ -276,6 +276,24 @@ sv_status sv_pack_drafts(const int32_t* tokens, const int32_t* counts, int32_t B
                          void* cuda_stream);
 
 /*
+ * Multi-candidate verification ("投机解码从零实现", §5.1 "批量验证": one
+ * target pass verifies several draft candidates, each returning its
+ * accepted tokens and gain). Flatten every request's candidates into one
+ * spec_verify call, each candidate its own request; request b owns
+ * candidates cu_cand[b] .. cu_cand[b+1]-1 of that call. This call then keeps
+ * per request the candidate with the longest committed length (lowest index
+ * among ties): best[b] is its index in the flattened call (-1 if the request
+ * had no candidate) and best_len[b] its out_len (0 then). All pointers are
+ * device arrays; asynchronous on `cuda_stream`.
+ *
+ * Keeping the longest of independently verified candidates raises the
+ * expected gain, but it does not preserve the target distribution: each
+ * candidate alone is lossless, the choice among them is not.
+ */
+sv_status sv_select_candidates(const int32_t* cu_cand, const int32_t* out_len, int32_t B,
+                               int32_t* best, int32_t* best_len, void* cuda_stream);
+
+/*
  * Acceptance statistics ("5.2 Draft 模型与无模型方案", §7.1 and §7.2),
  * accumulated on the device over any number of verify calls.
  *

@@ -268,3 +268,26 @@ class AdaptiveDraftLength:
             elif mean < self.target - 0.1:
                 self.k = max(self.min_k, self.k - 1)
         return self.k
+
+
+# ---------------------------------------------------------------------------
+# Multi-candidate verification: keep the candidate with the longest commit
+# ---------------------------------------------------------------------------
+def select_candidates(cu_cand, out_len):
+    """Request b owns candidates cu_cand[b] .. cu_cand[b+1]-1 (each verified
+    as its own request, "投机解码从零实现" §5.1 批量验证: one pass verifies
+    several drafts, each returning its accepted tokens and gain). The kept
+    candidate is the one with the longest committed length, the lowest index
+    among ties. Returns (best [B] global candidate index, or -1 for a
+    request without candidates; best_len [B], 0 then)."""
+    cu = [int(x) for x in cu_cand]
+    lens = [int(x) for x in out_len]
+    best, best_len = [], []
+    for b in range(len(cu) - 1):
+        bi, bl = -1, 0
+        for c in range(cu[b], cu[b + 1]):
+            if bi < 0 or lens[c] > bl:
+                bi, bl = c, lens[c]
+        best.append(bi)
+        best_len.append(bl)
+    return np.array(best, np.int32), np.array(best_len, np.int32)

@@ -104,3 +104,27 @@ def test_metrics_kernel_large_batch_and_clamping(cuda_lib, oracle_mod):
     api.sv_accumulate_metrics(torch.from_numpy(cu).cuda(), torch.from_numpy(lens).cuda(), m)
     torch.cuda.synchronize()
     _check_same(api.metrics_dict(m), oracle_mod.acceptance_metrics(cu, lens))
+
+
+@pytest.mark.gpu
+def test_select_candidates_after_a_flattened_verify(cuda_lib, oracle_mod):
+    """Requests with 0..5 candidates, each candidate verified as its own
+    request; the kept candidate matches the oracle's rule on the GPU's own
+    lengths, and the flattened verify matches the oracle."""
+    import parity
+    rng = np.random.default_rng(70)
+    B = 40
+    M = rng.integers(0, 6, size=B)
+    cu_cand = np.concatenate([[0], np.cumsum(M)]).astype(np.int32)
+    C = int(cu_cand[-1])
+    flat = W.gaussian_sampling(seed=71, B=C, K=rng.integers(1, 7, size=C).astype(np.int32), V=5000,
+                               sigma=1.0, draft_sigma=0.3, T=1.0, dtype="bf16")
+    db = parity.to_device(flat)
+    tok, ln, pr = api.spec_verify(db.target, db.draft, db.draft_tokens, db.cu_draft, db.uniforms,
+                                  db.temperature)
+    best, best_len = api.sv_select_candidates(torch.from_numpy(cu_cand).cuda(), ln)
+    torch.cuda.synchronize()
+    parity.compare(flat, (tok.cpu().numpy(), ln.cpu().numpy(), pr.cpu().numpy()), parity.oracle_verify(flat))
+    want_b, want_l = oracle_mod.select_candidates(cu_cand, ln.cpu().numpy())
+    assert np.array_equal(best.cpu().numpy(), want_b) and np.array_equal(best_len.cpu().numpy(), want_l)
+    assert (want_b == -1).sum() == (M == 0).sum()

@@ -514,3 +514,10 @@ def test_filtered_verify_is_lossless_for_the_filtered_target(oracle_mod):
     dof = int(keep.sum()) - 1
     from scipy.stats import chi2 as chi2_dist
     assert chi2 < chi2_dist.ppf(0.999, dof), (chi2, dof)
+
+
+def test_select_candidates_worked_example(oracle_mod):
+    """Three requests: candidates (2, 5, 5) keep the first 5; (1) keeps it;
+    none gives -1."""
+    best, best_len = oracle_mod.select_candidates([0, 3, 4, 4], [2, 5, 5, 1])
+    assert best.tolist() == [1, 3, -1] and best_len.tolist() == [5, 1, 0]
