@@ -291,3 +291,58 @@ def select_candidates(cu_cand, out_len):
         best.append(bi)
         best_len.append(bl)
     return np.array(best, np.int32), np.array(best_len, np.int32)
+
+
+# ---------------------------------------------------------------------------
+# Suffix proposer: frequency-ranked continuation ("5.2 Draft 模型与无模型方案",
+# §5.1-5.2 Suffix Decoding), plain Python
+# ---------------------------------------------------------------------------
+def suffix_propose(histories, hist_len, min_n: int, max_n: int, max_tokens: int,
+                   min_share: float = 0.5, max_occ: int = 256):
+    """For each history: the longest tail h[L-n, L) (n from min(max_n, L) down
+    to min_n) that occurs earlier, with the same admissible starts as the
+    n-gram proposer (0 <= s <= L-2n-1, so a continuation token precedes the
+    tail); the max_occ most recent occurrences vote. Step j: every
+    occurrence still in agreement whose continuation h[s+n+j] lies before the
+    tail votes for that token; the most frequent token wins (ties: the token
+    of the most recent voter). From the second step on, the proposal stops
+    when the winner holds less than min_share of the votes (dispersed
+    continuations); the occurrences that voted for the winner go on.
+    Returns (out_tokens [B, max_tokens] (-1 padded), count [B], n [B])."""
+    histories = np.asarray(histories)
+    B = histories.shape[0]
+    share = float(np.float32(min_share))
+    out = np.full((B, max(max_tokens, 0)), -1, np.int32)
+    cnt = np.zeros(B, np.int32)
+    nn = np.zeros(B, np.int32)
+    for b in range(B):
+        L = int(hist_len[b])
+        h = [int(x) for x in histories[b, :L]]
+        occ, n = [], 0
+        for m in range(min(max_n, L), min_n - 1, -1):
+            tail = h[L - m:L]
+            occ = [s for s in range(L - 2 * m - 1, -1, -1) if h[s:s + m] == tail]  # most recent first
+            if occ:
+                n = m
+                break
+        if not occ:
+            continue
+        active = occ[:max_occ]
+        props = []
+        for j in range(max_tokens):
+            votes = [(s, h[s + n + j]) for s in active if s + n + j < L - n]
+            if not votes:
+                break
+            count, recent = {}, {}
+            for s, t in votes:
+                count[t] = count.get(t, 0) + 1
+                recent.setdefault(t, s)  # votes run most recent first
+            win = max(count, key=lambda t: (count[t], recent[t]))
+            if j > 0 and float(count[win]) < share * float(len(votes)):
+                break
+            props.append(win)
+            active = [s for s, t in votes if t == win]
+        out[b, :len(props)] = props
+        cnt[b] = len(props)
+        nn[b] = n
+    return out, cnt, nn

@@ -521,3 +521,60 @@ def test_select_candidates_worked_example(oracle_mod):
     none gives -1."""
     best, best_len = oracle_mod.select_candidates([0, 3, 4, 4], [2, 5, 5, 1])
     assert best.tolist() == [1, 3, -1] and best_len.tolist() == [5, 1, 0]
+
+
+# --------------------------------------------------------------------------
+# Suffix proposer ("5.2 Draft 模型与无模型方案", §5.1-5.2)
+# --------------------------------------------------------------------------
+def test_suffix_prefers_the_frequent_continuation(oracle_mod):
+    """The page's case: after a suffix, "return" 20 times and "raise" twice."""
+    rng = np.random.default_rng(80)
+    S, RET, RAISE = [7, 8, 9], 100, 101
+    h = []
+    conts = [RET] * 20 + [RAISE] * 2
+    rng.shuffle(conts)
+    conts[-1] = RAISE  # the most recent occurrence says "raise"
+    for t in conts:
+        h += list(rng.integers(1000, 2000, size=5)) + S + [t]
+    h += S
+    out, cnt, n = oracle_mod.suffix_propose(np.array([h], np.int32), [len(h)], 3, 3, 4)
+    assert n[0] == 3 and out[0, 0] == RET
+    o2, c2, _ = oracle_mod.ngram_propose(np.array([h], np.int32), [len(h)], 3, 3, 4)
+    assert o2[0, 0] == RAISE  # the n-gram proposer copies the most recent match
+
+
+def test_suffix_length_follows_the_agreement(oracle_mod):
+    """Four occurrences continue S 100 50, S 100 50, S 100 60, S 100 70: the
+    second step has 2 of 4 votes."""
+    S = [7, 8, 9]
+    h = []
+    for tail in ([100, 50], [100, 50], [100, 60], [100, 70]):
+        h += [300, 301] + S + tail
+    h += S
+    H = np.array([h], np.int32)
+    out, cnt, _ = oracle_mod.suffix_propose(H, [len(h)], 3, 3, 5, min_share=0.5)
+    assert out[0, :2].tolist() == [100, 50]       # 2/4 >= 0.5 goes on
+    out, cnt, _ = oracle_mod.suffix_propose(H, [len(h)], 3, 3, 5, min_share=0.6)
+    assert cnt[0] == 1 and out[0, 0] == 100        # 2/4 < 0.6 stops
+    # ties: 60 and 70 once each after 100 -> among [100, 60] / [100, 70] the most recent
+    h2 = []
+    for tail in ([100, 60], [100, 70]):
+        h2 += [300, 301] + S + tail
+    h2 += S
+    out, cnt, _ = oracle_mod.suffix_propose(np.array([h2], np.int32), [len(h2)], 3, 3, 5, min_share=0.5)
+    assert out[0, :2].tolist() == [100, 70]
+
+
+def test_suffix_with_one_occurrence_is_the_ngram_proposer(oracle_mod):
+    """max_occ = 1 and min_share = 0: only the most recent match votes, so the
+    proposal is the n-gram proposer's (pinned to the page's printed cases)."""
+    rng = np.random.default_rng(81)
+    B, stride = 200, 60
+    hist = rng.integers(0, 4, size=(B, stride)).astype(np.int32)
+    hl = rng.integers(0, 61, size=B).astype(np.int32)
+    for mn, mx, mt in [(1, 3, 5), (2, 4, 2), (3, 3, 6)]:
+        a = oracle_mod.suffix_propose(hist, hl, mn, mx, mt, min_share=0.0, max_occ=1)
+        g = oracle_mod.ngram_propose(hist, hl, mn, mx, mt)
+        assert np.array_equal(a[1], g[1]) and np.array_equal(a[2], g[2])
+        for b in range(B):
+            assert np.array_equal(a[0][b, :a[1][b]], g[0][b, :g[1][b]])
