@@ -41,8 +41,8 @@ WORKLOAD = ("sampling verify B=256 K=7 V=151936 bf16 T=0.7, peaked rank-score ro
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per verify launch on this workload from one ncu
 # capture, valid only for the kernel sources whose hash is recorded with it.
-TRAFFIC = {"sources_sha256": "5eb80d66fd47183888fe31656b105c4a552e5b49418b5153f8daaf171d2fc9e2",
-           "bytes_per_launch": 1236312000 + 3829248,
+TRAFFIC = {"sources_sha256": "617dc6d706612d1a5f285cce4a33f66d0b0c017a8f2aee5e4564a590836fd87b",
+           "bytes_per_launch": 1235967000 + 3822336,
            "profile": "profiles/verify_kernel_sampling_B256_K7_V151936_bf16.md"}
 
 
@@ -383,6 +383,8 @@ EXTRA_WORKLOADS = {
                   "x̂ = argmax w.p. 0.7",
     "ngram_b128": "ngram_propose over 128 histories x 8192 int32 tokens (V=32000) with planted copies "
                   "covering 30%, n=3, up to 5 tokens",
+    "suffix_b128": "suffix_propose (frequency-ranked, min_share 0.5, up to 256 voters) over the same 128 "
+                   "histories x 8192 int32 tokens, n=3, up to 5 tokens",
     "onehot_b128": "verify of the n-gram proposals (one-hot q), fp32 z ~ N(0,2^2), V=32000, T=1.0",
     "ragged_b512": "ragged mixed verify B=512 K_b~U{1..8} V=256000 bf16 T=1.0, half greedy requests",
     "metrics_b512": "acceptance statistics of 512 verify rounds (K_b~U{1..8}) added to a device "
@@ -393,6 +395,7 @@ EXTRA_WORKLOADS = {
                         "256 requests, then the longest commit kept per request",
 }
 FILTER_K, FILTER_P = 50, 0.9
+SUFFIX_SHARE, SUFFIX_OCC = 0.5, 256
 
 
 def _extra_setup(name, seed):
@@ -404,8 +407,9 @@ def _extra_setup(name, seed):
     from speculative_decoding_verification_27_gb300 import api
     from speculative_decoding_verification_27_gb300 import workloads as W
 
-    if name == "ngram_b128":
+    if name in ("ngram_b128", "suffix_b128"):
         import oracle
+        suffix = name == "suffix_b128"
         nb = W.config4_histories(seed=seed)
         h = torch.from_numpy(nb.histories).cuda()
         hl = torch.from_numpy(nb.hist_len).cuda()
@@ -417,13 +421,21 @@ def _extra_setup(name, seed):
         outs = [out, cnt, nn]
 
         def step():
-            api.ngram_propose(h, hl, nb.min_n, nb.max_n, nb.max_tokens, out_tokens=out, out_count=cnt,
-                              out_n=nn)
+            if suffix:
+                api.suffix_propose(h, hl, nb.min_n, nb.max_n, nb.max_tokens, SUFFIX_SHARE, SUFFIX_OCC,
+                                   out_tokens=out, out_count=cnt, out_n=nn)
+            else:
+                api.ngram_propose(h, hl, nb.min_n, nb.max_n, nb.max_tokens, out_tokens=out, out_count=cnt,
+                                  out_n=nn)
 
         def oracle_fn():
             t = time.perf_counter()
-            o = oracle.ngram_propose(nb.histories, nb.hist_len, nb.min_n, nb.max_n, nb.max_tokens)
-            return time.perf_counter() - t, 1, o  # the oracle's n-gram search is single-threaded
+            if suffix:
+                o = oracle.suffix_propose(nb.histories, nb.hist_len, nb.min_n, nb.max_n, nb.max_tokens,
+                                          min_share=SUFFIX_SHARE, max_occ=SUFFIX_OCC)
+            else:
+                o = oracle.ngram_propose(nb.histories, nb.hist_len, nb.min_n, nb.max_n, nb.max_tokens)
+            return time.perf_counter() - t, 1, o  # the oracle's proposers are single-threaded
 
         def check(o):
             return {"histories": int(h.shape[0]),
@@ -433,6 +445,8 @@ def _extra_setup(name, seed):
                                           np.arange(nb.max_tokens)[None] < o[1][:, None], o[0], -1)))}
         desc = {"B": int(h.shape[0]), "L": int(nb.histories.shape[1]), "n": nb.max_n,
                 "max_tokens": nb.max_tokens}
+        if suffix:
+            desc.update(min_share=SUFFIX_SHARE, max_occ=SUFFIX_OCC)
         return (desc, host, outs, step, int(h.shape[0]), "histories/s", int(nb.histories.nbytes),
                 True, oracle_fn, check)
 
@@ -623,7 +637,7 @@ def run_extra(args):
     line = {
         "metric": METRIC, "value": units / (ms * 1e-3), "unit": unit, "n_gpus": 1, "steps": n,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "i32" if args.workload in ("ngram_b128", "metrics_b512") else "f32",
+        "vs_baseline": None, "dtype": "i32" if args.workload in ("ngram_b128", "suffix_b128", "metrics_b512") else "f32",
         "data": "synthetic",
         "config": dict({"workload": EXTRA_WORKLOADS[args.workload],
                         "l2": "before each timed launch a 256 MB buffer is written and another "
@@ -632,12 +646,13 @@ def run_extra(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
                      "note": {"ngram_b128": "latency-bound: one CTA per history",
+                              "suffix_b128": "latency-bound: one CTA per history",
                               "metrics_b512": "latency-bound: 4 KB of inputs"}.get(args.workload)},
         "e2e": {"value": units / (e_ms * 1e-3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e_ms},
         "gpu_launches": n,
         "clocks": clocks,
-        "cpu_baseline": {"value": (units if args.workload in ("ngram_b128", "verify_b1", "greedy_b64",
+        "cpu_baseline": {"value": (units if args.workload in ("ngram_b128", "suffix_b128", "verify_b1", "greedy_b64",
                                                             "onehot_b128", "metrics_b512")
                                    else spot["rows"]) / dt,
                          "unit": unit, "cores": threads, "kind": "oracle",

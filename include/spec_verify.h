@@ -266,7 +266,40 @@ sv_status ngram_propose(const int32_t* histories, int64_t hist_stride, const int
                         void* cuda_stream);
 
 /*
- * Glue from ngram_propose to spec_verify: cu_draft[B+1] = exclusive prefix
+ * Frequency-ranked suffix proposer ("5.2 Draft 模型与无模型方案", §5
+ * "Suffix Decoding"): §5.1 ranks the continuations seen after a suffix by
+ * how often they occur, and warns that dispersed continuations make long
+ * proposals unwise; §5.2 makes the configured length a ceiling, not a fixed
+ * length. The page prescribes no algorithm; this is the reading:
+ *   - the tail is the longest h[L-n, L), n = min(max_n, L) down to min_n,
+ *     with an earlier occurrence at some start s, 0 <= s <= L-2n-1 (the
+ *     starts ngram_propose admits); the max_occ occurrences with the largest
+ *     s are the voters;
+ *   - step j = 0, 1, ...: each voter whose continuation token h[s+n+j] lies
+ *     before the tail (s+n+j < L-n) votes for it; the token with the most
+ *     votes is proposed (among equal counts, the token of the voter with the
+ *     largest s); for j >= 1 the proposal ends instead when the winner's
+ *     votes are fewer than min_share x the votes cast (compared in double
+ *     precision, min_share widened from float); only the winner's voters
+ *     vote in the next step; the proposal ends at max_tokens or when no
+ *     voter is left.
+ * With max_occ = 1 and min_share = 0 the result is ngram_propose's.
+ *
+ *   histories, hist_len, B, min_n, max_n, max_tokens, out_tokens, out_count,
+ *   out_n: as for ngram_propose (rows padded with -1; out_n = 0 and
+ *   out_count = 0 without a match).
+ *   min_share   in [0, 1]; max_occ in [1, SV_SUFFIX_MAX_OCC].
+ * Bit-exact. No workspace. Histories with hist_stride <= 16384 are staged in
+ * shared memory; longer ones are read from global memory.
+ */
+#define SV_SUFFIX_MAX_OCC 256
+sv_status suffix_propose(const int32_t* histories, int64_t hist_stride, const int32_t* hist_len,
+                         int32_t B, int32_t min_n, int32_t max_n, int32_t max_tokens,
+                         float min_share, int32_t max_occ, int32_t* out_tokens,
+                         int32_t* out_count, int32_t* out_n, void* cuda_stream);
+
+/*
+ * Glue from ngram_propose (or suffix_propose) to spec_verify: cu_draft[B+1] = exclusive prefix
  * sums of counts[B] (clamped to [0, max_tokens]), and the proposals of
  * tokens[B, max_tokens] packed to packed[cu_draft[b] + i] (capacity
  * B * max_tokens). One launch on the stream.

@@ -207,6 +207,33 @@ def ngram_propose(histories: torch.Tensor, hist_len: torch.Tensor, min_n: int, m
     return out_tokens, out_count, out_n
 
 
+SV_SUFFIX_MAX_OCC = 256
+
+
+def suffix_propose(histories: torch.Tensor, hist_len: torch.Tensor, min_n: int, max_n: int,
+                   max_tokens: int, min_share: float = 0.5, max_occ: int = SV_SUFFIX_MAX_OCC, *,
+                   out_tokens=None, out_count=None, out_n=None, stream=None):
+    """Frequency-ranked suffix proposer. Returns (out_tokens [B, max_tokens], out_count, out_n)."""
+    lib = load()
+    fn = lib.suffix_propose
+    P, i32 = ctypes.c_void_p, ctypes.c_int32
+    fn.argtypes = [P, ctypes.c_int64, P, i32, i32, i32, i32, ctypes.c_float, i32, P, P, P, P]
+    fn.restype = ctypes.c_int
+    B, stride = histories.shape
+    dev = histories.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, max_tokens), dtype=torch.int32, device=dev)
+    if out_count is None:
+        out_count = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_n is None:
+        out_n = torch.empty(B, dtype=torch.int32, device=dev)
+    st = fn(_ptr(histories), int(stride), _ptr(hist_len), int(B), int(min_n), int(max_n),
+            int(max_tokens), float(min_share), int(max_occ), _ptr(out_tokens), _ptr(out_count),
+            _ptr(out_n), _stream(stream))
+    _check("suffix_propose", st)
+    return out_tokens, out_count, out_n
+
+
 def sv_pack_drafts(tokens: torch.Tensor, counts: torch.Tensor, max_tokens: int, *, cu_draft=None,
                    packed=None, stream=None):
     """(cu_draft [B+1], packed [B*max_tokens]) from padded proposals and their counts."""

@@ -163,6 +163,11 @@ sv_status ngram_propose(const int32_t* histories, int64_t hist_stride, const int
   if (hist_stride > 0x7fffffffLL) return SV_ERR_INVALID_ARG;
   const int staged = hist_stride <= sv::kNgSmemInts ? 1 : 0;
   const size_t smem = staged ? (size_t)hist_stride * sizeof(int32_t) : 0;
+  // Static and dynamic shared memory together above 48 KB need the
+  // function's opt-in (a full 12288-token stage plus the static words).
+  if (smem > 0 && cudaFuncSetAttribute(sv::ngram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)(sv::kNgSmemInts * sizeof(int32_t))) != cudaSuccess)
+    return SV_ERR_CUDA;
   sv::ngram_kernel<<<(unsigned)B, sv::kNgThreads, smem, static_cast<cudaStream_t>(cuda_stream)>>>(
       histories, (long long)hist_stride, hist_len, min_n, max_n, max_tokens, out_tokens, out_count,
       out_n, staged);

@@ -92,6 +92,22 @@ def test_ngram_and_pack_host_validation(lib):
     assert ng(mt=-1) == E
     assert ng(stride=-1) == E
     assert lib.ngram_propose(MISALIGNED, 16, FAKE, 2, 1, 3, 5, FAKE, FAKE, FAKE, None) == E
+    fn = lib.suffix_propose
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p] + [ctypes.c_int32] * 4 + \
+        [ctypes.c_float, ctypes.c_int32] + [ctypes.c_void_p] * 4
+    sf = lambda B=2, mn=1, mx=3, mt=5, share=0.5, occ=256, h=FAKE: fn(h, 16, FAKE, B, mn, mx, mt, share, occ,
+                                                                     FAKE, FAKE, FAKE, None)
+    assert sf(B=0) == api.SV_OK
+    assert sf(B=-1) == E
+    assert sf(mn=0) == E
+    assert sf(mn=3, mx=2) == E
+    assert sf(mt=-1) == E
+    assert sf(occ=0) == E
+    assert sf(occ=257) == E
+    assert sf(share=-0.1) == E
+    assert sf(share=1.5) == E
+    assert sf(share=float("nan")) == E
+    assert sf(h=MISALIGNED) == E
     assert lib.sv_pack_drafts(FAKE, FAKE, -1, 5, FAKE, FAKE, None) == E
     assert lib.sv_pack_drafts(FAKE, FAKE, 2, 5, None, FAKE, None) == E
     bits = ctypes.c_uint32(0)
