@@ -20,11 +20,23 @@
 // keeps its own histogram in shared memory, and a thread merges runs of
 // equal digits in its vector before adding, because logits of one row share
 // few leading digits.
+//
+// With top-k for k <= 256 a row is read from global memory once. Every
+// logit at or above a floor is appended to a buffer in shared memory, and
+// the floor never exceeds the k-th largest logit seen so far, so the buffer
+// always holds the row's top-k set. The first floor is the k-th largest of
+// the 256 threads' maxima over the first chunk (k of those maxima lie at or
+// above it). If the buffer could overflow in the next chunk, the floor rises
+// to the k-th largest value in the buffer and the buffer is compacted. After
+// the pass, the radix levels above run on the buffer alone. A row whose tie
+// group at the floor does not fit falls back to the passes over the row.
 #include "../../include/spec_verify.h"
 #include "sv_filter.cuh"
 
 #include <cmath>
 #include <cstdint>
+#include <cstring>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace sv {
@@ -50,17 +62,27 @@ __device__ __forceinline__ float value32(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-constexpr int kCand = 4096;  // logits that shared memory holds once few keys are left in play
+constexpr int kCand = 4096;      // logits that shared memory holds once few keys are left in play
+constexpr int kStreamK = 256;    // top-k up to this collects its candidates in one pass
+constexpr int kChunkWords = 4;   // 16-byte words a thread holds per chunk of the one-pass collection
 
 struct FtSmem {
   unsigned cnt[kFtWarps][256];
   float mass[kFtWarps][256];
-  double tc[256], tm[256];  // per-digit count and mass totals
+  unsigned tc[256];          // per-digit counts
+  double tm[256];            // per-digit mass totals (mass levels only)
   float wmax[kFtWarps];
+  unsigned wcount[kFtWarps];
   float cand[kCand];        // the logits still in play, once they fit
   unsigned ncand;
+  float wm[2][kFtWarps];      // per-warp running reference and mass (one-pass top-p bound)
+  float wsf[2][kFtWarps];
+  double wsd[kFtWarps];       // per-warp mass in double (end of the one-pass top-p)
+  double row_mass;            // one-pass top-p: mass left out of the buffer, relative to 2^row_ref
+  float row_ref;              // one-pass top-p: the row's integer mass reference (log2 units)
   uint32_t digit;
-  double before_c, before_m;  // count and mass of the digits above the chosen one
+  unsigned before_c;          // count of the digits above the chosen one
+  double before_m;            // and their mass (mass levels)
   double total_m;
   float rowmax;
 };
@@ -196,13 +218,16 @@ __device__ void histogram(FtSmem& s, const Src& src, int shift, uint32_t prefix,
     if (lane == 0) s.wmax[warp] = vmax;
   }
   __syncthreads();
-  double tc = 0.0, tm = 0.0;
-  for (int w = 0; w < kFtWarps; ++w) {
-    tc += (double)s.cnt[w][tid];
-    tm += (double)s.mass[w][tid];
-  }
+  // Counts stay integers; only mass levels pay for double precision (the
+  // FP64 pipe is narrow on this part).
+  unsigned tc = 0u;
+  for (int w = 0; w < kFtWarps; ++w) tc += s.cnt[w][tid];
   s.tc[tid] = tc;
-  s.tm[tid] = tm;
+  if (by_mass) {
+    double tm = 0.0;
+    for (int w = 0; w < kFtWarps; ++w) tm += (double)s.mass[w][tid];
+    s.tm[tid] = tm;
+  }
   if (tid == 0 && track_max) {
     float r = s.wmax[0];
     for (int w = 1; w < kFtWarps; ++w) r = fmaxf(r, s.wmax[w]);
@@ -219,43 +244,61 @@ __device__ void histogram(FtSmem& s, const Src& src, int shift, uint32_t prefix,
   __syncthreads();
 }
 
-// The first digit from the top at which the running count (or mass) reaches
-// `need`: s.digit, with the count and mass of the digits above it in
-// s.before_c / s.before_m. If rounding leaves `need` unreached, the lowest
-// digit is taken (everything in play stays).
-__device__ void pick_digit(FtSmem& s, double need, bool by_mass) {
+// The first digit from the top at which the running count reaches need_c
+// (count levels) or the running mass reaches need_m (mass levels): s.digit,
+// with the count and mass of the digits above it in s.before_c /
+// s.before_m, taken from the warp's scans. If rounding leaves need_m
+// unreached, the lowest digit is taken (everything in play stays).
+__device__ void pick_digit(FtSmem& s, unsigned need_c, double need_m, bool by_mass) {
   const int lane = threadIdx.x & 31;
   if (threadIdx.x < 32) {
-    const double* t = by_mass ? s.tm : s.tc;
     // Lane l covers digits 255 - 8l .. 248 - 8l (from the top).
-    double loc[8], sum = 0.0;
+    unsigned lc[8], csum = 0u;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      loc[j] = t[255 - 8 * lane - j];
-      sum += loc[j];
+      lc[j] = s.tc[255 - 8 * lane - j];
+      csum += lc[j];
     }
-    double incl = sum;
+    unsigned cincl = csum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
+      const unsigned n = __shfl_up_sync(0xffffffffu, cincl, o);
+      if (lane >= o) cincl += n;
     }
-    const unsigned hit = __ballot_sync(0xffffffffu, incl >= need);
+    unsigned cexcl = __shfl_up_sync(0xffffffffu, cincl, 1);
+    if (lane == 0) cexcl = 0u;
+    double lm[8], mincl = 0.0, mexcl = 0.0;
+    if (by_mass) {
+      double msum = 0.0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        lm[j] = s.tm[255 - 8 * lane - j];
+        msum += lm[j];
+      }
+      mincl = msum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double n = __shfl_up_sync(0xffffffffu, mincl, o);
+        if (lane >= o) mincl += n;
+      }
+      mexcl = __shfl_up_sync(0xffffffffu, mincl, 1);
+      if (lane == 0) mexcl = 0.0;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) lm[j] = 0.0;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, by_mass ? mincl >= need_m : cincl >= need_c);
     const int first = hit ? __ffs(hit) - 1 : 31;
     if (lane == first) {
-      double run = incl - sum;
+      unsigned bc = cexcl;
+      double bm = mexcl;
       int j = 0;
       for (; j < 7; ++j) {
-        if (run + loc[j] >= need) break;
-        run += loc[j];
+        if (by_mass ? bm + lm[j] >= need_m : bc + lc[j] >= need_c) break;
+        bc += lc[j];
+        bm += lm[j];
       }
-      const uint32_t d = 255u - 8u * (uint32_t)lane - (uint32_t)j;
-      double bc = 0.0, bm = 0.0;
-      for (uint32_t e = d + 1; e < 256; ++e) {
-        bc += s.tc[e];
-        bm += s.tm[e];
-      }
-      s.digit = d;
+      s.digit = 255u - 8u * (uint32_t)lane - (uint32_t)j;
       s.before_c = bc;
       s.before_m = bm;
     }
@@ -278,6 +321,409 @@ __device__ void collect(FtSmem& s, const RowSrc<DT>& row, uint32_t lo) {
   __syncthreads();
 }
 
+// One thread's share of chunk c of the one-pass collection: kChunkWords
+// 16-byte words, word u at index (c * kChunkWords + u) * kFtThreads + tid of
+// the row viewed as 16-byte words; logits past V read as -inf.
+template <int DT>
+__device__ __forceinline__ void load_chunk(const void* row, int V, bool vec, int c,
+                                           uint4 (&w)[kChunkWords]) {
+  constexpr int EV = DT == 1 ? 8 : 4;  // logits per 16-byte word
+  constexpr uint32_t kNegInf = DT == 1 ? 0xff80ff80u : 0xff800000u;
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int u = 0; u < kChunkWords; ++u) {
+    const int j = (c * kChunkWords + u) * kFtThreads + tid;
+    const int e0 = j * EV;
+    if (vec) {
+      // V * s is a multiple of 16 bytes: a word is wholly inside or outside.
+      w[u] = e0 < V ? __ldg(reinterpret_cast<const uint4*>(row) + j)
+                    : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
+    } else {
+      uint32_t ws[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (DT == 1) {
+          const uint16_t* r = static_cast<const uint16_t*>(row);
+          const int e = e0 + 2 * q;
+          const uint32_t lo = e < V ? __ldg(r + e) : 0xff80u;
+          const uint32_t hi = e + 1 < V ? __ldg(r + e + 1) : 0xff80u;
+          ws[q] = lo | (hi << 16);
+        } else {
+          const float* r = static_cast<const float*>(row);
+          const int e = e0 + q;
+          ws[q] = e < V ? __float_as_uint(__ldg(r + e)) : kNegInf;
+        }
+      }
+      w[u] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+    }
+  }
+}
+
+// The k-th largest key among one key per thread (1 <= k <= kFtThreads): the
+// largest T with at least k keys >= T, one bit at a time from the top.
+template <int DT>
+__device__ __forceinline__ uint32_t kth_key_of_threads(uint32_t key, int k) {
+  constexpr int KB = DT == 1 ? 16 : 32;
+  uint32_t T = 0u;
+  for (int bit = KB - 1; bit >= 0; --bit) {
+    const uint32_t t = T | (1u << bit);
+    if (__syncthreads_count(key >= t) >= k) T = t;
+  }
+  return T;
+}
+
+// A key as a floor value; keys below -inf's (NaN patterns) keep everything.
+template <int DT>
+__device__ __forceinline__ float floor_value(uint32_t T) {
+  constexpr uint32_t kKeyNegInf = DT == 1 ? 0x007fu : 0x007fffffu;
+  if (T <= kKeyNegInf) return -INFINITY;
+  return DT == 1 ? value16(T) : value32(T);
+}
+
+// Exact k-th largest key of the buffer (s.cand[0, s.ncand)) by the radix
+// levels, then a stable in-place compaction to the values >= it. The new
+// floor goes to `fl`; returns the number of values kept (the same in every
+// thread, so callers branch on it without reading shared memory again).
+template <int DT>
+__device__ int raise_floor(FtSmem& s, int k, float& fl_out) {
+  constexpr int KB = DT == 1 ? 16 : 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = (int)s.ncand;
+  const CandSrc<DT> cs{s.cand, n};
+  uint32_t prefix = 0u;
+  unsigned need = (unsigned)k;
+  for (int sh = KB - 8; sh >= 0; sh -= 8) {
+    histogram<DT>(s, cs, sh, prefix, sh == KB - 8, 0u, false, 0.f, 0.f, false);
+    pick_digit(s, need, 0.0, false);
+    need -= s.before_c;
+    prefix = (prefix << 8) | s.digit;
+  }
+  const float fl = floor_value<DT>(prefix);
+  // Round r reads entries [256 r, 256 r + 256) before any write of the round;
+  // a kept entry moves to a position at or below its own.
+  int out = 0;
+  for (int base = 0; base < n; base += kFtThreads) {
+    const int j = base + tid;
+    const float v = j < n ? s.cand[j] : -INFINITY;
+    const bool keep = j < n && v >= fl;
+    const unsigned bal = __ballot_sync(0xffffffffu, keep);
+    if (lane == 0) s.wcount[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kFtWarps; ++w) {
+      const int c = (int)s.wcount[w];
+      before += w < warp ? c : 0;
+      total += c;
+    }
+    if (keep) s.cand[out + before + __popc(bal & ((1u << lane) - 1u))] = v;
+    out += total;
+    __syncthreads();
+  }
+  if (tid == 0) s.ncand = (unsigned)out;
+  __syncthreads();
+  fl_out = fl;
+  return out;
+}
+
+// 32-bit word q of a thread's chunk share (two bf16 logits or one fp32).
+__device__ __forceinline__ uint32_t word_at(const uint4 (&w)[kChunkWords], int q) {
+  const uint4 x = w[q >> 2];
+  const int r = q & 3;
+  return r == 0 ? x.x : (r == 1 ? x.y : (r == 2 ? x.z : x.w));
+}
+
+// Packed bf16 pairs: per-half (a >= b) as 0xffff masks, and the per-half maximum.
+__device__ __forceinline__ uint32_t bf2_ge_mask(uint32_t a, uint32_t b) {
+  __nv_bfloat162 x, y;
+  memcpy(&x, &a, 4);
+  memcpy(&y, &b, 4);
+  return __hge2_mask(x, y);
+}
+__device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
+  __nv_bfloat162 x, y;
+  memcpy(&x, &a, 4);
+  memcpy(&y, &b, 4);
+  const __nv_bfloat162 r = __hmax2(x, y);
+  uint32_t u;
+  memcpy(&u, &r, 4);
+  return u;
+}
+
+// Running state of the one-pass collection, per thread.
+//   top-k: rmax is the running maximum.
+//   top-p: masses are kept relative to 2^ref with ref an integer (log2
+//   units, ref >= rmax * cc), so that moving to a larger reference is an
+//   exact power-of-two rescale. sum_all is the mass of every logit seen (for
+//   the floor); sum_rest the mass of those not appended, in double (the
+//   row's mass is the buffer's, summed later exactly as the nucleus walk
+//   sums it, plus this).
+struct StreamState {
+  float fl;         // floor: logits >= fl are appended
+  uint32_t fl2;     // bf16: the floor in both halves
+  float rmax;       // running maximum
+  float ref;        // top-p: integer reference, or -inf before any finite logit
+  float sum_all;    // top-p: mass of every logit seen, relative to 2^ref
+  double sum_rest;  // top-p: mass of the logits not appended, relative to 2^ref
+};
+
+// Raises the floor to f. bf16 rows round f down to a bf16 value first, so
+// that the packed compare (fl2) and the float compare (fl) agree.
+template <int DT>
+__device__ __forceinline__ void set_floor(StreamState& st, float f) {
+  if (DT == 1) {
+    const uint32_t u = __float_as_uint(f);
+    uint32_t hi = u & 0xffff0000u;
+    if ((u & 0x80000000u) && (u & 0xffffu)) hi += 0x10000u;  // negative: away from zero
+    f = __uint_as_float(hi);
+  }
+  st.fl = fmaxf(st.fl, f);
+  const uint32_t fb = __float_as_uint(st.fl) >> 16;
+  st.fl2 = fb | (fb << 16);
+}
+
+// (reference, mass) over the warp: the mass rescaled to the warp's largest
+// reference by powers of two.
+__device__ __forceinline__ void warp_ref_mass(float& ref, float& sm) {
+  float wr = ref;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) wr = fmaxf(wr, __shfl_xor_sync(0xffffffffu, wr, o));
+  sm = ref > -INFINITY ? ldexpf(sm, (int)(ref - wr)) : 0.f;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+  ref = wr;
+}
+
+// The top-p floor from the warps' (reference, mass) in slot `slot`: every
+// logit whose mass is below (1 - p) S / V lies outside the nucleus
+// (together they weigh less than (1 - p) S), and S only grows as the pass
+// goes on. The 0.05 in log2 units keeps the bound below the exact one
+// despite fp32 sums.
+__device__ __forceinline__ float top_p_floor(const FtSmem& s, int slot, float p, float cc, int V) {
+  float R = -INFINITY, S = 0.f;
+#pragma unroll
+  for (int w = 0; w < kFtWarps; ++w) R = fmaxf(R, s.wm[slot][w]);
+  if (!(R > -INFINITY)) return -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kFtWarps; ++w)
+    if (s.wm[slot][w] > -INFINITY) S += ldexpf(s.wsf[slot][w], (int)(s.wm[slot][w] - R));
+  return (R + log2f((1.f - p) * S / (float)V) - 0.05f) / cc;
+}
+
+// Appends this thread's logits of chunk c that are >= the floor (logits past
+// V excepted). my_end: the largest buffer end this thread's appends reached;
+// my_ovf: a logit found the buffer full and was dropped.
+template <int DT>
+__device__ __forceinline__ void append_chunk(FtSmem& s, const uint4 (&cur)[kChunkWords], int c, int V,
+                                             const StreamState& st, unsigned& my_end, bool& my_ovf) {
+  constexpr int EV = DT == 1 ? 8 : 4;
+  constexpr int NW = kChunkWords * 4;
+#pragma unroll
+  for (int q = 0; q < NW; ++q) {
+    const uint32_t wq = word_at(cur, q);
+    const int j = (c * kChunkWords + (q >> 2)) * kFtThreads + threadIdx.x;  // 16-byte word
+    if (DT == 1) {
+      const uint32_t mk = bf2_ge_mask(wq, st.fl2);
+      if (mk) {
+        const int e = j * EV + 2 * (q & 3);
+        const bool a = (mk & 0xffffu) && e < V, b = (mk >> 16) && e + 1 < V;
+        const unsigned n = (unsigned)a + (unsigned)b;
+        if (n) {
+          unsigned pos = atomicAdd(&s.ncand, n);
+          my_end = max(my_end, pos + n);
+          if (pos + n <= (unsigned)kCand) {
+            if (a) s.cand[pos++] = __uint_as_float(wq << 16);
+            if (b) s.cand[pos] = __uint_as_float(wq & 0xffff0000u);
+          } else {
+            my_ovf = true;
+          }
+        }
+      }
+    } else {
+      const float z = __uint_as_float(wq);
+      if (z >= st.fl && j * EV + (q & 3) < V) {
+        const unsigned pos = atomicAdd(&s.ncand, 1u);
+        my_end = max(my_end, pos + 1u);
+        if (pos < (unsigned)kCand)
+          s.cand[pos] = z;
+        else
+          my_ovf = true;
+      }
+    }
+  }
+}
+
+// Mass of this thread's chunk share relative to 2^ref: of every logit
+// (all), and of those the floor leaves out (rest). Padding (-inf) weighs 0.
+template <int DT>
+__device__ __forceinline__ void chunk_mass(const uint4 (&cur)[kChunkWords], const StreamState& st,
+                                           float cc, bool with_floor, float& all, float& rest) {
+  constexpr int NW = kChunkWords * 4;
+  all = 0.f;
+  rest = 0.f;
+#pragma unroll
+  for (int q = 0; q < NW; ++q) {
+    const uint32_t wq = word_at(cur, q);
+#pragma unroll
+    for (int h = 0; h < (DT == 1 ? 2 : 1); ++h) {
+      const float z = DT == 1 ? __uint_as_float(h ? (wq & 0xffff0000u) : (wq << 16)) : __uint_as_float(wq);
+      const float m = exp2f(fmaf(z, cc, -st.ref));
+      all += m;
+      // Padding is -inf (mass 0), so the V bound does not matter here.
+      if (!with_floor || z < st.fl) rest += m;
+    }
+  }
+}
+
+// One step of the one-pass collection: chunk c, held in `cur`, while the
+// next chunk loads into `nxt`. Returns false when the collection must give
+// up (the caller then takes the passes over the row).
+template <int DT>
+__device__ __forceinline__ bool stream_step(FtSmem& s, const void* row, int V, bool vec, int k, float p,
+                                            float cc, int c, int nch, const uint4 (&cur)[kChunkWords],
+                                            uint4 (&nxt)[kChunkWords], StreamState& st) {
+  constexpr int NW = kChunkWords * 4;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (c + 1 < nch) load_chunk<DT>(row, V, vec, c + 1, nxt);
+  // This thread's chunk maximum.
+  float cmax;
+  if (DT == 1) {
+    uint32_t m2 = word_at(cur, 0);
+#pragma unroll
+    for (int q = 1; q < NW; ++q) m2 = bf2_max(m2, word_at(cur, q));
+    cmax = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xffff0000u));
+  } else {
+    cmax = __uint_as_float(word_at(cur, 0));
+#pragma unroll
+    for (int q = 1; q < NW; ++q) cmax = fmaxf(cmax, __uint_as_float(word_at(cur, q)));
+  }
+  if (k > 0) {
+    // k of the threads' running maxima lie at or above their k-th largest.
+    if (c < 16) {
+      st.rmax = fmaxf(st.rmax, cmax);
+      if (((c + 1) & c) == 0) set_floor<DT>(st, floor_value<DT>(kth_key_of_threads<DT>(key_of<DT>(st.rmax), k)));
+    }
+  } else {
+    // Move the reference up (an exact power-of-two rescale) if this chunk
+    // holds a larger maximum.
+    const float nm = fmaxf(st.rmax, cmax);
+    if (nm > -INFINITY) {
+      const float nref = ceilf(nm * cc);
+      if (!(st.ref >= nref)) {
+        if (st.ref > -INFINITY) {
+          const int d = (int)(st.ref - nref);
+          st.sum_all = ldexpf(st.sum_all, d);
+          st.sum_rest = ldexp(st.sum_rest, d);
+        }
+        st.ref = nref;
+      }
+      st.rmax = nm;
+    }
+    if (c == 0) {
+      // The first chunk's floor comes from the first chunk itself.
+      float all = 0.f, rest = 0.f;
+      if (st.ref > -INFINITY) chunk_mass<DT>(cur, st, cc, false, all, rest);
+      float r = st.ref, sm = all;
+      warp_ref_mass(r, sm);
+      if (lane == 0) {
+        s.wm[0][warp] = r;
+        s.wsf[0][warp] = sm;
+      }
+      __syncthreads();
+      set_floor<DT>(st, top_p_floor(s, 0, p, cc, V));
+    }
+    if (st.ref > -INFINITY) {
+      float all, rest;
+      chunk_mass<DT>(cur, st, cc, true, all, rest);
+      st.sum_all += all;
+      st.sum_rest += (double)rest;
+    }
+  }
+  unsigned my_end = 0u;
+  bool my_ovf = false;
+  if (cmax >= st.fl) append_chunk<DT>(s, cur, c, V, st, my_end, my_ovf);
+  if (k == 0 && c > 0) {
+    float r = st.ref, sm = st.sum_all;
+    warp_ref_mass(r, sm);
+    if (lane == 0) {
+      s.wm[c & 1][warp] = r;
+      s.wsf[c & 1][warp] = sm;
+    }
+  }
+  // Every decision below comes from a barrier's own result or from values
+  // all threads hold: other threads may already be appending the next chunk
+  // while a thread would still read the counter.
+  if (__syncthreads_or(my_end > (unsigned)(kCand / 2))) {
+    if (__syncthreads_or(my_ovf)) return false;
+    if (k > 0 && c + 1 < nch) {
+      float f;
+      const int kept = raise_floor<DT>(s, k, f);
+      set_floor<DT>(st, f);
+      if (kept > kCand / 2) return false;
+    }
+  }
+  if (k == 0 && c > 0 && c + 1 < nch) set_floor<DT>(st, top_p_floor(s, c & 1, p, cc, V));
+  return true;
+}
+
+// One pass over the row that leaves in s.cand every logit at or above the
+// final floor, the floor at most the row's threshold:
+//   top-k (k >= 1, k <= kStreamK): the floor is raised after chunks 0, 1, 3,
+//     7 and 15 to the k-th largest of the threads' running maxima, and to the
+//     k-th largest value in the buffer when the buffer passes half full;
+//   top-p alone (k = 0, 0 < p < 1): the floor is (R + log2((1-p) S / V)) / cc
+//     from the running reference R and mass S. The row's maximum, its
+//     reference and the mass of the logits left out of the buffer (double,
+//     relative to 2^reference) land in s.rowmax, s.row_ref, s.row_mass.
+// Returns false when the buffer cannot hold the logits at the floor.
+template <int DT>
+__device__ bool stream_collect(FtSmem& s, const void* row, int V, bool vec, int k, float p, float cc) {
+  constexpr int EV = DT == 1 ? 8 : 4;
+  constexpr int CH = kChunkWords * EV * kFtThreads;  // logits per chunk
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nch = (V + CH - 1) / CH;
+  if (threadIdx.x == 0) s.ncand = 0u;
+  StreamState st{-INFINITY, 0xff80ff80u, -INFINITY, -INFINITY, 0.f, 0.0};
+  uint4 a[kChunkWords], b[kChunkWords];
+  load_chunk<DT>(row, V, vec, 0, a);
+  for (int c = 0; c < nch; c += 2) {
+    if (!stream_step<DT>(s, row, V, vec, k, p, cc, c, nch, a, b, st)) return false;
+    if (c + 1 < nch && !stream_step<DT>(s, row, V, vec, k, p, cc, c + 1, nch, b, a, st)) return false;
+  }
+  if (k == 0) {
+    float m = st.rmax, r = st.ref;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, o));
+    }
+    double d = st.ref > -INFINITY ? ldexp(st.sum_rest, (int)(st.ref - r)) : 0.0;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+    if (lane == 0) {
+      s.wm[0][warp] = m;
+      s.wsf[0][warp] = r;
+      s.wsd[warp] = d;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float M = -INFINITY, R = -INFINITY;
+      for (int w = 0; w < kFtWarps; ++w) {
+        M = fmaxf(M, s.wm[0][w]);
+        R = fmaxf(R, s.wsf[0][w]);
+      }
+      double S = 0.0;
+      for (int w = 0; w < kFtWarps; ++w)
+        if (s.wsf[0][w] > -INFINITY) S += ldexp(s.wsd[w], (int)(s.wsf[0][w] - R));
+      s.rowmax = M;
+      s.row_ref = R;
+      s.row_mass = S;
+    }
+    __syncthreads();
+  }
+  return true;
+}
+
 template <int DT>
 __device__ float row_threshold(FtSmem& s, const void* rowp, int V, bool vec, int top_k, float top_p,
                                float c) {
@@ -289,22 +735,27 @@ __device__ float row_threshold(FtSmem& s, const void* rowp, int V, bool vec, int
   bool in_smem = false;  // the candidates hold every key still in play
   uint32_t floor = 0u;   // keys >= floor are kept
   float M = -INFINITY;
+  bool mass_known = false;  // s.row_mass holds the row's mass relative to M
   if (use_k) {
+    if (top_k <= kStreamK && stream_collect<DT>(s, rowp, V, vec, top_k, 1.f, c)) {
+      cs.n = (int)s.ncand;
+      in_smem = true;
+    }
     uint32_t prefix = 0u;
-    double need = (double)top_k, above = 0.0;
+    unsigned need = (unsigned)top_k, above = 0u;
     for (int sh = KB - 8; sh >= 0; sh -= 8) {
       const bool top = sh == KB - 8;
       if (in_smem)
-        histogram<DT>(s, cs, sh, prefix, top, 0u, false, 0.f, 0.f, false);
+        histogram<DT>(s, cs, sh, prefix, top, 0u, false, 0.f, 0.f, top);
       else
         histogram<DT>(s, row, sh, prefix, top, 0u, false, 0.f, 0.f, top);
       if (top) M = s.rowmax;
-      pick_digit(s, need, false);
+      pick_digit(s, need, 0.0, false);
       need -= s.before_c;
       above += s.before_c;
       prefix = (prefix << 8) | s.digit;
-      const double in_play = above + s.tc[s.digit];
-      if (!in_smem && in_play <= (double)kCand && (sh > 0 || use_p)) {
+      const unsigned in_play = above + s.tc[s.digit];
+      if (!in_smem && in_play <= (unsigned)kCand && (sh > 0 || use_p)) {
         collect<DT>(s, row, prefix << sh);
         cs.n = (int)s.ncand;
         in_smem = true;
@@ -314,26 +765,38 @@ __device__ float row_threshold(FtSmem& s, const void* rowp, int V, bool vec, int
   }
   if (use_p) {
     if (!use_k) {
-      histogram<DT>(s, row, KB - 8, 0u, true, 0u, false, 0.f, 0.f, true);  // the row maximum
+      if (stream_collect<DT>(s, rowp, V, vec, 0, top_p, c)) {
+        cs.n = (int)s.ncand;
+        in_smem = true;
+        mass_known = true;
+      } else {
+        histogram<DT>(s, row, KB - 8, 0u, true, 0u, false, 0.f, 0.f, true);  // the row maximum
+      }
       M = s.rowmax;
     }
     if (!(M > -INFINITY)) return -INFINITY;
-    const float mc = __fmul_rn(M, c);
+    // Masses are relative to 2^mc: the row maximum's scaled value, or the
+    // one-pass collection's integer reference, which its left-out mass
+    // shares.
+    const float mc = mass_known ? s.row_ref : __fmul_rn(M, c);
     uint32_t prefix = 0u;
-    double need = 0.0, above = 0.0;
+    double need = 0.0;
+    unsigned above = 0u;
     for (int sh = KB - 8; sh >= 0; sh -= 8) {
       const bool top = sh == KB - 8;
       if (in_smem)
         histogram<DT>(s, cs, sh, prefix, top, floor, true, c, mc, false);
       else
         histogram<DT>(s, row, sh, prefix, top, floor, true, c, mc, false);
-      if (top) need = (double)top_p * s.total_m;
-      pick_digit(s, need, true);
+      // The buffer of the one-pass top-p holds only the logits near the
+      // top: the mass the pass left out of it is added to the buffer's.
+      if (top) need = (double)top_p * (mass_known ? s.total_m + s.row_mass : s.total_m);
+      pick_digit(s, 0u, need, true);
       need -= s.before_m;
       above += s.before_c;
       prefix = (prefix << 8) | s.digit;
-      const double in_play = above + s.tc[s.digit];
-      if (!in_smem && sh > 0 && in_play <= (double)kCand) {
+      const unsigned in_play = above + s.tc[s.digit];
+      if (!in_smem && sh > 0 && in_play <= (unsigned)kCand) {
         collect<DT>(s, row, prefix << sh);
         cs.n = (int)s.ncand;
         in_smem = true;
@@ -348,8 +811,9 @@ __device__ float row_threshold(FtSmem& s, const void* rowp, int V, bool vec, int
 // Rows [0, R_t) are target rows (request b at cu[b] + b + i); rows
 // [R_t, R_t + R_d) draft rows. Greedy requests keep everything.
 template <int DT>
-__global__ void __launch_bounds__(kFtThreads) threshold_kernel(FtParams P) {
-  __shared__ FtSmem s;
+__global__ void __launch_bounds__(kFtThreads, 3) threshold_kernel(FtParams P) {
+  extern __shared__ __align__(16) unsigned char ft_smem[];
+  FtSmem& s = *reinterpret_cast<FtSmem*>(ft_smem);
   // Rows past the caller's arrays (offsets that the verify kernel will
   // reject) are skipped.
   int R_d = P.cu[P.B], R_t = R_d + P.B;
@@ -360,7 +824,7 @@ __global__ void __launch_bounds__(kFtThreads) threshold_kernel(FtParams P) {
     const bool is_t = r < R_t;
     const int rr = is_t ? r : r - R_t;
     // The row's request, for its mode.
-    int lo = 0, hi = P.B - 1;
+    int lo = 0, hi = P.mode ? P.B - 1 : 0;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if ((is_t ? P.cu[mid] + mid : P.cu[mid]) <= rr)
@@ -379,20 +843,31 @@ __global__ void __launch_bounds__(kFtThreads) threshold_kernel(FtParams P) {
   }
 }
 
+template <int DT>
+static cudaError_t launch_thresholds_t(const FtParams& P, int sms, cudaStream_t st) {
+  const size_t smem = sizeof(FtSmem);
+  cudaError_t e = cudaFuncSetAttribute(threshold_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, threshold_kernel<DT>, kFtThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  // One wave of resident CTAs walks the rows.
+  const int rows = 2 * P.rows_t;
+  int grid = rows < per_sm * sms ? rows : per_sm * sms;
+  if (grid < 1) grid = 1;
+  threshold_kernel<DT><<<grid, kFtThreads, smem, st>>>(P);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_thresholds(const FtParams& P, int dtype, cudaStream_t st) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int rows = 2 * P.rows_t;
-  int grid = rows < 4 * sms ? rows : 4 * sms;
-  if (grid < 1) grid = 1;
-  if (dtype == SV_BF16)
-    threshold_kernel<1><<<grid, kFtThreads, 0, st>>>(P);
-  else
-    threshold_kernel<0><<<grid, kFtThreads, 0, st>>>(P);
-  return cudaGetLastError();
+  return dtype == SV_BF16 ? launch_thresholds_t<1>(P, sms, st) : launch_thresholds_t<0>(P, sms, st);
 }
 
 }  // namespace sv

@@ -88,3 +88,39 @@ def test_filtered_bad_offsets_stay_in_bounds(cuda_lib):
     torch.cuda.synchronize()
     fb = api.spec_verify_filtered_workspace_size(b.B, b.R_t, b.V) - api.spec_verify_workspace_size(b.B, b.R_t, b.V)
     assert api.sv_check_status(ws[fb:]) & api.SV_DATA_BAD_OFFSETS
+
+
+def _shaped_rows(shape, R, V, rng):
+    """Rows that push the threshold kernel's one-pass collection to its
+    edges: rising values pass every chunk's floor (a compaction per chunk),
+    falling values pass almost nothing after the first chunk, and constant or
+    two-valued rows leave a tie group at the floor that does not fit (the
+    passes over the row take over)."""
+    x = np.arange(V, dtype=np.float64)
+    if shape == "ascending":
+        z = np.tile(-6.0 + 12.0 * x / V, (R, 1)) + rng.normal(0, 0.01, (R, V))
+    elif shape == "descending":
+        z = np.tile(6.0 - 12.0 * x / V, (R, 1)) + rng.normal(0, 0.01, (R, V))
+    elif shape == "constant":
+        z = np.zeros((R, V))
+    else:  # two levels, the high one in the second half
+        z = np.where(x[None, :] >= V // 2, 1.0, 0.0) + np.zeros((R, 1))
+    return z.astype(np.float32)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("shape", ["ascending", "descending", "constant", "two_levels"])
+@pytest.mark.parametrize("top_k,top_p", [(50, 1.0), (256, 0.9), (257, 0.8), (1, 0.5), (0, 0.9), (0, 0.5)])
+def test_one_pass_collection_edges(cuda_lib, dtype, shape, top_k, top_p):
+    rng = np.random.default_rng(560 + top_k)
+    V = 40000
+    b = W.gaussian_sampling(seed=561 + top_k, B=6, K=2, V=V, sigma=2.0, draft_sigma=0.5, T=1.0)
+    zt = _shaped_rows(shape, b.R_t, V, rng)
+    zd = zt[np.concatenate([np.arange(b.cu_draft[i] + i, b.cu_draft[i] + i + 2) for i in range(b.B)])]
+    zd = zd + rng.normal(0, 0.3, zd.shape).astype(np.float32)
+    if dtype == "bf16":
+        b.target, b.draft = W.to_bf16_bits(zt), W.to_bf16_bits(zd)
+    else:
+        b.target, b.draft = zt, zd.astype(np.float32)
+    rep = _run(b, top_k, top_p)
+    assert rep.mismatched_requests <= 1
