@@ -66,9 +66,13 @@ constexpr int kCand = 4096;      // logits that shared memory holds once few key
 constexpr int kStreamK = 256;    // top-k up to this collects its candidates in one pass
 constexpr int kChunkWords = 4;   // 16-byte words a thread holds per chunk of the one-pass collection
 
+constexpr int kHistCopies = 2;  // per-pair-of-warps histogram copies
+constexpr int kRing = 3;        // chunks of the one-pass collection in shared memory (two in flight)
+
 struct FtSmem {
-  unsigned cnt[kFtWarps][256];
-  float mass[kFtWarps][256];
+  uint4 ring[kRing][kChunkWords][kFtThreads];  // thread t's words of a chunk at [.][u][t]
+  unsigned cnt[kHistCopies][256];
+  double mass[kHistCopies][256];  // mass bins in double: the nucleus cut compares sums of hundreds of terms
   unsigned tc[256];          // per-digit counts
   double tm[256];            // per-digit mass totals (mass levels only)
   float wmax[kFtWarps];
@@ -182,19 +186,20 @@ template <int DT, class Src>
 __device__ void histogram(FtSmem& s, const Src& src, int shift, uint32_t prefix, bool top_level,
                           uint32_t floor, bool by_mass, float c, float mc, bool track_max) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int k = tid; k < kFtWarps * 256; k += kFtThreads) {
+  for (int k = tid; k < kHistCopies * 256; k += kFtThreads) {
     (&s.cnt[0][0])[k] = 0u;
-    (&s.mass[0][0])[k] = 0.f;
+    (&s.mass[0][0])[k] = 0.0;
   }
   __syncthreads();
   // Runs of one digit are merged in registers before they reach shared memory.
   uint32_t run_d = 0xffffffffu;
   unsigned run_n = 0;
-  float run_m = 0.f, vmax = -INFINITY;
+  double run_m = 0.0;
+  float vmax = -INFINITY;
   auto flush = [&]() {
     if (run_n) {
-      atomicAdd(&s.cnt[warp][run_d], run_n);
-      if (by_mass) atomicAdd(&s.mass[warp][run_d], run_m);
+      atomicAdd(&s.cnt[warp & (kHistCopies - 1)][run_d], run_n);
+      if (by_mass) atomicAdd(&s.mass[warp & (kHistCopies - 1)][run_d], run_m);
     }
   };
   src.each([&](uint32_t key, float v) {
@@ -206,10 +211,10 @@ __device__ void histogram(FtSmem& s, const Src& src, int shift, uint32_t prefix,
       flush();
       run_d = d;
       run_n = 0;
-      run_m = 0.f;
+      run_m = 0.0;
     }
     ++run_n;
-    if (by_mass) run_m += exp2f(fmaf(v, c, -mc));
+    if (by_mass) run_m += (double)exp2f(fmaf(v, c, -mc));
   });
   flush();
   if (track_max) {
@@ -221,11 +226,11 @@ __device__ void histogram(FtSmem& s, const Src& src, int shift, uint32_t prefix,
   // Counts stay integers; only mass levels pay for double precision (the
   // FP64 pipe is narrow on this part).
   unsigned tc = 0u;
-  for (int w = 0; w < kFtWarps; ++w) tc += s.cnt[w][tid];
+  for (int w = 0; w < kHistCopies; ++w) tc += s.cnt[w][tid];
   s.tc[tid] = tc;
   if (by_mass) {
     double tm = 0.0;
-    for (int w = 0; w < kFtWarps; ++w) tm += (double)s.mass[w][tid];
+    for (int w = 0; w < kHistCopies; ++w) tm += s.mass[w][tid];
     s.tm[tid] = tm;
   }
   if (tid == 0 && track_max) {
@@ -321,12 +326,14 @@ __device__ void collect(FtSmem& s, const RowSrc<DT>& row, uint32_t lo) {
   __syncthreads();
 }
 
-// One thread's share of chunk c of the one-pass collection: kChunkWords
-// 16-byte words, word u at index (c * kChunkWords + u) * kFtThreads + tid of
-// the row viewed as 16-byte words; logits past V read as -inf.
+// Starts the copy of this thread's share of chunk c into ring stage
+// c % kRing: kChunkWords 16-byte words, word u at index
+// (c * kChunkWords + u) * kFtThreads + tid of the row viewed as 16-byte
+// words; logits past V read as -inf. Vector rows copy asynchronously
+// (cp.async, completed by the caller's wait); other rows load and store.
+// Each thread reads back only its own words, so no barrier is involved.
 template <int DT>
-__device__ __forceinline__ void load_chunk(const void* row, int V, bool vec, int c,
-                                           uint4 (&w)[kChunkWords]) {
+__device__ __forceinline__ void issue_chunk(FtSmem& s, const void* row, int V, bool vec, int c) {
   constexpr int EV = DT == 1 ? 8 : 4;  // logits per 16-byte word
   constexpr uint32_t kNegInf = DT == 1 ? 0xff80ff80u : 0xff800000u;
   const int tid = threadIdx.x;
@@ -334,10 +341,17 @@ __device__ __forceinline__ void load_chunk(const void* row, int V, bool vec, int
   for (int u = 0; u < kChunkWords; ++u) {
     const int j = (c * kChunkWords + u) * kFtThreads + tid;
     const int e0 = j * EV;
+    uint4* slot = &s.ring[c % kRing][u][tid];
     if (vec) {
       // V * s is a multiple of 16 bytes: a word is wholly inside or outside.
-      w[u] = e0 < V ? __ldg(reinterpret_cast<const uint4*>(row) + j)
-                    : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
+      if (e0 < V) {
+        const unsigned dst = (unsigned)__cvta_generic_to_shared(slot);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst),
+                     "l"(reinterpret_cast<const uint4*>(row) + j)
+                     : "memory");
+      } else {
+        *slot = make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
+      }
     } else {
       uint32_t ws[4];
 #pragma unroll
@@ -354,10 +368,15 @@ __device__ __forceinline__ void load_chunk(const void* row, int V, bool vec, int
           ws[q] = e < V ? __float_as_uint(__ldg(r + e)) : kNegInf;
         }
       }
-      w[u] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+      *slot = make_uint4(ws[0], ws[1], ws[2], ws[3]);
     }
   }
 }
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+// All but the most recent group of this thread's copies have landed.
+__device__ __forceinline__ void cp_async_wait_but_one() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 // The k-th largest key among one key per thread (1 <= k <= kFtThreads): the
 // largest T with at least k keys >= T, one bit at a time from the top.
@@ -576,15 +595,13 @@ __device__ __forceinline__ void chunk_mass(const uint4 (&cur)[kChunkWords], cons
 }
 
 // One step of the one-pass collection: chunk c, held in `cur`, while the
-// next chunk loads into `nxt`. Returns false when the collection must give
-// up (the caller then takes the passes over the row).
+// next two chunks are on their way. Returns false when the collection must
+// give up (the caller then takes the passes over the row).
 template <int DT>
-__device__ __forceinline__ bool stream_step(FtSmem& s, const void* row, int V, bool vec, int k, float p,
-                                            float cc, int c, int nch, const uint4 (&cur)[kChunkWords],
-                                            uint4 (&nxt)[kChunkWords], StreamState& st) {
+__device__ __forceinline__ bool stream_step(FtSmem& s, int V, int k, float p, float cc, int c, int nch,
+                                            const uint4 (&cur)[kChunkWords], StreamState& st) {
   constexpr int NW = kChunkWords * 4;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (c + 1 < nch) load_chunk<DT>(row, V, vec, c + 1, nxt);
   // This thread's chunk maximum.
   float cmax;
   if (DT == 1) {
@@ -684,11 +701,22 @@ __device__ bool stream_collect(FtSmem& s, const void* row, int V, bool vec, int 
   const int nch = (V + CH - 1) / CH;
   if (threadIdx.x == 0) s.ncand = 0u;
   StreamState st{-INFINITY, 0xff80ff80u, -INFINITY, -INFINITY, 0.f, 0.0};
-  uint4 a[kChunkWords], b[kChunkWords];
-  load_chunk<DT>(row, V, vec, 0, a);
-  for (int c = 0; c < nch; c += 2) {
-    if (!stream_step<DT>(s, row, V, vec, k, p, cc, c, nch, a, b, st)) return false;
-    if (c + 1 < nch && !stream_step<DT>(s, row, V, vec, k, p, cc, c + 1, nch, b, a, st)) return false;
+  // Chunks c + 1 and c + 2 are in flight while chunk c is processed.
+  issue_chunk<DT>(s, row, V, vec, 0);
+  cp_async_commit();
+  if (nch > 1) issue_chunk<DT>(s, row, V, vec, 1);
+  cp_async_commit();
+  for (int c = 0; c < nch; ++c) {
+    cp_async_wait_but_one();
+    uint4 cur[kChunkWords];
+#pragma unroll
+    for (int u = 0; u < kChunkWords; ++u) cur[u] = s.ring[c % kRing][u][threadIdx.x];
+    if (c + 2 < nch) issue_chunk<DT>(s, row, V, vec, c + 2);
+    cp_async_commit();
+    if (!stream_step<DT>(s, V, k, p, cc, c, nch, cur, st)) {
+      cp_async_wait_all();
+      return false;
+    }
   }
   if (k == 0) {
     float m = st.rmax, r = st.ref;
