@@ -1358,7 +1358,7 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
           for (int v = 0; v < kVPT; ++v) tv[v] *= f;
           int t;
           const float tot = warp_tile_totals(tv, lane, t);
-          const int l = k * kVPT + t;
+          const int l = (c0 + k) * kVPT + t;  // tile of the row (a part starts at chunk c0)
           if ((lane & (32 / kVPT - 1)) == 0 && l < ntiles) s.wtot[l * kWarps + warp] = tot;
           if (lane == 0) bref[k * kWarps + warp] = ref;
         });
@@ -1389,21 +1389,26 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
     double Sp, Sq;
     combine_softmax<EPV>(at, ad, has_d, P.c, s, mcp, Sp, mcq, Sq);
     if (VEC && btiles && ok) {
-      // Tile sums of r = 2^(z c - mc_p): each warp's part rescaled from its
-      // chunk offset to the row's, summed over the warps in fp64.
+      // Tile sums of r = 2^(z c - mc_p) over this slice's tiles: each warp's
+      // part rescaled from its chunk offset to the slice's, summed over the
+      // warps in fp64. (A split row's merge rescales them to the row's.)
       if (tid == 0) s.bcast_f[0] = mcp;
       __syncthreads();
       const float M = s.bcast_f[0];
       constexpr int TILE = kThreads * EPV;
       const int ntiles = (V + TILE - 1) / TILE;
       const float* bref = reinterpret_cast<const float*>(s.tincl);
-      if (tid < ntiles) {
+      const int l = c0 * kVPT + tid;
+      if (tid < (c1 - c0) * kVPT && l < ntiles) {
         const int k = tid / kVPT;
         double T = 0.0;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w)
-          T += (double)(s.wtot[tid * kWarps + w] * ex2(bref[k * kWarps + w] - M));
-        P.btile[(size_t)b * P.tsum_stride + tid] = T;
+        for (int w = 0; w < kWarps; ++w) {
+          const float r = bref[k * kWarps + w];
+          if (r > -INFINITY) T += (double)(s.wtot[l * kWarps + w] * ex2(r - M));
+        }
+        P.btile[(size_t)b * P.tsum_stride + l] = T;
+        __threadfence();  // visible to a split row's merging CTA before this part counts as done
       }
       if (tid == 0) s.btile_ok = 1;
       __syncthreads();
@@ -1574,7 +1579,7 @@ __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int 
     c1 = min(nch, c0 + cpp);
   }
   PartRec st;
-  const bool btiles = VEC && part < 0 && i == K && !greedy;
+  const bool btiles = VEC && i == K && !greedy;
   if (!slice_stats<DT, VEC>(P, s, ring, trow, drow, greedy, c0, c1, st, btiles, b)) return false;
   if (part >= 0) {
     if (tid == 0) {
@@ -1591,7 +1596,27 @@ __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int 
     if (!s.merge) return true;
     if (tid < 32) {
       const PartRec m = merge_parts(P.parts + (size_t)split * np, np);
-      if (tid == 0) st = m;
+      if (tid == 0) {
+        st = m;
+        s.bcast_f[0] = m.mc_p;
+      }
+    }
+    if (btiles) {
+      // Each part left its tiles' sums relative to its own offset: rescale
+      // them to the merged one, as merge_parts does with the parts' sums.
+      __syncthreads();
+      const float M = s.bcast_f[0];
+      constexpr int TILE = kThreads * Elem<DT & 1>::kEPV;
+      const int ntiles = (P.V + TILE - 1) / TILE;
+      const int cpp = (nch + np - 1) / np;
+      for (int l = tid; l < ntiles; l += kThreads) {
+        const PartRec* pr = P.parts + (size_t)split * np + (l / kVPT) / cpp;
+        const double Sp_part = __ldcg(&pr->S_p);
+        const float f = Sp_part > 0.0 ? ex2(__ldcg(&pr->mc_p) - M) : 0.f;
+        double* bt = P.btile + (size_t)b * P.tsum_stride + l;
+        *bt = __ldcg(bt) * (double)f;
+      }
+      if (tid == 0) s.btile_ok = 1;
     }
   }
   if (tid == 0) decide_row<DT>(P, s, t, st);
