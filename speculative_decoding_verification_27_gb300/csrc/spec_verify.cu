@@ -37,6 +37,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <cuda_bf16.h>
 
 #include "../../include/spec_verify.h"
 #include "sv_device.cuh"
@@ -361,6 +362,14 @@ struct SoftAcc {
   }
 };
 
+// Per-half (a >= b) of two bf16 pairs as 0xffff masks.
+__device__ __forceinline__ uint32_t bf16x2_ge_mask(uint32_t a, uint32_t b) {
+  __nv_bfloat162 x, y;
+  memcpy(&x, &a, 4);
+  memcpy(&y, &b, 4);
+  return __hge2_mask(x, y);
+}
+
 // The kVPT vectors this thread consumes from a ring stage holding elements
 // [x, x + kVPT * kThreads * EPV) of a row: whole vectors inside the row are
 // read, those at or past V read as -inf.
@@ -370,12 +379,14 @@ __device__ __forceinline__ uint4 mask_below(uint4 v, float tau) {
   if constexpr ((DT & kFilt) == 0) {
     return v;
   } else if constexpr ((DT & 1) == 1) {
+    // Packed compare of bf16 pairs against tau in both halves (a bf16 row's
+    // threshold is an exact bf16 value), then -inf where it fails.
+    const uint32_t tb = __float_as_uint(tau) >> 16, t2 = tb | (tb << 16);
     uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint32_t lo = __uint_as_float(w[q] << 16) >= tau ? (w[q] & 0xffffu) : 0xff80u;
-      const uint32_t hi = __uint_as_float(w[q] & 0xffff0000u) >= tau ? (w[q] & 0xffff0000u) : 0xff800000u;
-      w[q] = hi | lo;
+      const uint32_t mk = bf16x2_ge_mask(w[q], t2);
+      w[q] = (w[q] & mk) | (0xff80ff80u & ~mk);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
   } else {
@@ -424,6 +435,23 @@ __device__ __forceinline__ void stage_vectors(uint32_t stage, int x, int V, uint
       const int vi = v * kThreads + tid;
       rv[v] = (x + vi * EPV < V) ? mask_below<DT>(lds16(stage + 16u * vi), tau) : make_uint4(n, n, n, n);
     }
+  }
+}
+
+// Filtered variants: whether any of this thread's vectors kept a logit (a
+// vector whose logits all fall below the threshold adds no mass and no
+// maximum, so its softmax update can be skipped). Always true otherwise.
+template <int DT>
+__device__ __forceinline__ bool any_kept(const uint4 (&rv)[kVPT]) {
+  if constexpr ((DT & kFilt) == 0) {
+    return true;
+  } else {
+    constexpr uint32_t n = Raw<DT & 1>::kNegInf;
+    bool any = false;
+#pragma unroll
+    for (int v = 0; v < kVPT; ++v)
+      any |= (rv[v].x != n) | (rv[v].y != n) | (rv[v].z != n) | (rv[v].w != n);
+    return any;
   }
 }
 
@@ -1371,11 +1399,11 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
             s.zx_p = pick_element<DT>(rv, vx, jx);
             s.zx_ok = 1;
           }
-          at.template add_raw<DT, kVPT>(rv, P.c);
+          if (any_kept<DT>(rv)) at.template add_raw<DT, kVPT>(rv, P.c);
           if (has_d) {
             stage_vectors<DT>(stage + kChunkBytes, x0 + k * CH, V, rv, s.tau_d);
             if (k == kx) s.zx_q = pick_element<DT>(rv, vx, jx);
-            ad.template add_raw<DT, kVPT>(rv, P.c);
+            if (any_kept<DT>(rv)) ad.template add_raw<DT, kVPT>(rv, P.c);
           }
         });
       }
