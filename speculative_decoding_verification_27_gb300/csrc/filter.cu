@@ -484,6 +484,8 @@ struct StreamState {
   float ref;        // top-p: integer reference, or -inf before any finite logit
   float sum_all;    // top-p: mass of every logit seen, relative to 2^ref
   double sum_rest;  // top-p: mass of the logits not appended, relative to 2^ref
+  unsigned my_end;  // largest buffer end of this thread's appends since the last checkpoint
+  bool my_ovf;      // an append since the last checkpoint found the buffer full
 };
 
 // Raises the floor to f. bf16 rows round f down to a bf16 value first, so
@@ -656,22 +658,25 @@ __device__ __forceinline__ bool stream_step(FtSmem& s, int V, int k, float p, fl
       st.sum_rest += (double)rest;
     }
   }
-  unsigned my_end = 0u;
-  bool my_ovf = false;
-  if (cmax >= st.fl) append_chunk<DT>(s, cur, c, V, st, my_end, my_ovf);
+  if (cmax >= st.fl) append_chunk<DT>(s, cur, c, V, st, st.my_end, st.my_ovf);
+  // Checkpoints after every second chunk (and the last): the buffer's fill,
+  // the floor raise and the top-p bound. Between them a chunk appends at
+  // most CH logits, and an append that finds the buffer full is caught here.
+  if (!(c & 1) && c + 1 < nch) return true;
+  const int slot = ((c >> 1) + 1) & 1;  // chunk 0's own bound used slot 0
   if (k == 0 && c > 0) {
     float r = st.ref, sm = st.sum_all;
     warp_ref_mass(r, sm);
     if (lane == 0) {
-      s.wm[c & 1][warp] = r;
-      s.wsf[c & 1][warp] = sm;
+      s.wm[slot][warp] = r;
+      s.wsf[slot][warp] = sm;
     }
   }
   // Every decision below comes from a barrier's own result or from values
   // all threads hold: other threads may already be appending the next chunk
   // while a thread would still read the counter.
-  if (__syncthreads_or(my_end > (unsigned)(kCand / 2))) {
-    if (__syncthreads_or(my_ovf)) return false;
+  if (__syncthreads_or(st.my_end > (unsigned)(kCand / 2))) {
+    if (__syncthreads_or(st.my_ovf)) return false;
     if (k > 0 && c + 1 < nch) {
       float f;
       const int kept = raise_floor<DT>(s, k, f);
@@ -679,7 +684,9 @@ __device__ __forceinline__ bool stream_step(FtSmem& s, int V, int k, float p, fl
       if (kept > kCand / 2) return false;
     }
   }
-  if (k == 0 && c > 0 && c + 1 < nch) set_floor<DT>(st, top_p_floor(s, c & 1, p, cc, V));
+  st.my_end = 0u;
+  st.my_ovf = false;
+  if (k == 0 && c > 0 && c + 1 < nch) set_floor<DT>(st, top_p_floor(s, slot, p, cc, V));
   return true;
 }
 
@@ -700,7 +707,7 @@ __device__ bool stream_collect(FtSmem& s, const void* row, int V, bool vec, int 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nch = (V + CH - 1) / CH;
   if (threadIdx.x == 0) s.ncand = 0u;
-  StreamState st{-INFINITY, 0xff80ff80u, -INFINITY, -INFINITY, 0.f, 0.0};
+  StreamState st{-INFINITY, 0xff80ff80u, -INFINITY, -INFINITY, 0.f, 0.0, 0u, false};
   // Chunks c + 1 and c + 2 are in flight while chunk c is processed.
   issue_chunk<DT>(s, row, V, vec, 0);
   cp_async_commit();
