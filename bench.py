@@ -41,8 +41,8 @@ WORKLOAD = ("sampling verify B=256 K=7 V=151936 bf16 T=0.7, peaked rank-score ro
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per verify launch on this workload from one ncu
 # capture, valid only for the kernel sources whose hash is recorded with it.
-TRAFFIC = {"sources_sha256": "617dc6d706612d1a5f285cce4a33f66d0b0c017a8f2aee5e4564a590836fd87b",
-           "bytes_per_launch": 1235967000 + 3822336,
+TRAFFIC = {"sources_sha256": "f4d5bc4d6180888943d4e785458afb9b72700198f7f5611239e16be0933b7ed0",
+           "bytes_per_launch": 1235410000 + 4466432,
            "profile": "profiles/verify_kernel_sampling_B256_K7_V151936_bf16.md"}
 
 
