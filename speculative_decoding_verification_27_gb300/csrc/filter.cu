@@ -65,6 +65,12 @@ __device__ __forceinline__ float value32(uint32_t k) {
 constexpr int kCand = 4096;      // logits that shared memory holds once few keys are left in play
 constexpr int kStreamK = 256;    // top-k up to this collects its candidates in one pass
 constexpr int kChunkWords = 4;   // 16-byte words a thread holds per chunk of the one-pass collection
+#ifndef SV_KTH_CHUNKS
+#define SV_KTH_CHUNKS 0x808Bu
+#endif
+// Chunks (bit c, c < 16) after which top-k raises its floor to the k-th
+// largest of the threads' running maxima: 0, 1, 3, 7 and 15 by default.
+constexpr unsigned kKthChunks = SV_KTH_CHUNKS;
 
 constexpr int kHistCopies = 2;  // per-pair-of-warps histogram copies
 constexpr int kRing = 3;        // chunks of the one-pass collection in shared memory (two in flight)
@@ -620,7 +626,7 @@ __device__ __forceinline__ bool stream_step(FtSmem& s, int V, int k, float p, fl
     // k of the threads' running maxima lie at or above their k-th largest.
     if (c < 16) {
       st.rmax = fmaxf(st.rmax, cmax);
-      if (((c + 1) & c) == 0) set_floor<DT>(st, floor_value<DT>(kth_key_of_threads<DT>(key_of<DT>(st.rmax), k)));
+      if ((kKthChunks >> c) & 1u) set_floor<DT>(st, floor_value<DT>(kth_key_of_threads<DT>(key_of<DT>(st.rmax), k)));
     }
   } else {
     // Move the reference up (an exact power-of-two rescale) if this chunk
