@@ -35,7 +35,7 @@
  *              before the current tail, non-empty continuation, truncated
  *              to max_tokens).
  *
- * Readings where the pages are silent (each one also listed in the design doc):
+ * Readings where the pages are silent:
  *   - accept iff u < min(1, p/q) with u a supplied uniform in [0,1);
  *   - the correction/bonus draw is the inverse CDF in vocabulary order:
  *     the smallest k with C_k > u' * Z, C_k = sum_{x<=k} r_x; if rounding
