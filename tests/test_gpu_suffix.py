@@ -142,3 +142,29 @@ def test_ngram_at_its_staging_limit(cuda_lib, oracle_mod, stride):
     g = out.cpu().numpy()
     for b in range(3):
         assert np.array_equal(g[b, :o_cnt[b]], o_out[b, :o_cnt[b]])
+
+
+def test_suffix_proposals_then_one_hot_verify(cuda_lib, oracle_mod):
+    """The proposer's pipeline: suffix proposals packed by sv_pack_drafts and
+    verified with one-hot q against fp32 target logits (V = 32000), against
+    the oracle's proposals and verify. Repetitive histories (8 distinct
+    tokens) make the votes matter."""
+    import parity
+    rng = np.random.default_rng(1200)
+    B, L, mt = 64, 2000, 5
+    hist = rng.integers(0, 8, size=(B, L)).astype(np.int32)
+    hl = rng.integers(L // 2, L + 1, size=B).astype(np.int32)
+    h, dl = torch.from_numpy(hist).cuda(), torch.from_numpy(hl).cuda()
+    out, cnt, nn = api.suffix_propose(h, dl, 2, 3, mt, 0.6, 256)
+    cu, packed = api.sv_pack_drafts(out, cnt, mt)
+    torch.cuda.synchronize()
+    o_out, o_cnt, o_n = oracle_mod.suffix_propose(hist, hl, 2, 3, mt, min_share=0.6, max_occ=256)
+    assert np.array_equal(cnt.cpu().numpy(), o_cnt) and np.array_equal(nn.cpu().numpy(), o_n)
+    assert np.array_equal(out.cpu().numpy(), o_out)
+    assert ((o_cnt > 0) & (o_cnt < mt)).sum() > 10  # many proposals end early on split votes
+    vb = W.config4_verify(seed=1201, proposals=o_out, counts=o_cnt)
+    assert np.array_equal(cu.cpu().numpy(), vb.cu_draft)
+    assert np.array_equal(packed.cpu().numpy()[:vb.R_d], vb.draft_tokens)
+    db = parity.to_device(vb)
+    rep = parity.compare(vb, parity.gpu_verify(db), parity.oracle_verify(vb))
+    assert rep.mismatched_requests <= max(1, 1e-4 * rep.rows)
