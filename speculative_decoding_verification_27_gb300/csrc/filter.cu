@@ -78,7 +78,12 @@ constexpr int kRing = 3;        // chunks of the one-pass collection in shared m
 struct FtSmem {
   uint4 ring[kRing][kChunkWords][kFtThreads];  // thread t's words of a chunk at [.][u][t]
   unsigned cnt[kHistCopies][256];
-  double mass[kHistCopies][256];  // mass bins in double: the nucleus cut compares sums of hundreds of terms
+  // Mass bins in fixed point (units of 2^-44): every mass is at most ~1
+  // (relative to the row maximum or the integer reference), so its fp32
+  // value times 2^44 converts exactly (to the unit for masses below 2^-20),
+  // a row of at most 2^19 logits fits in 64 bits, and the sums are exact in
+  // any order. The nucleus cut compares them against the 1e-6 flag margin.
+  unsigned long long mass[kHistCopies][256];
   unsigned tc[256];          // per-digit counts
   double tm[256];            // per-digit mass totals (mass levels only)
   float wmax[kFtWarps];
@@ -194,13 +199,13 @@ __device__ void histogram(FtSmem& s, const Src& src, int shift, uint32_t prefix,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int k = tid; k < kHistCopies * 256; k += kFtThreads) {
     (&s.cnt[0][0])[k] = 0u;
-    (&s.mass[0][0])[k] = 0.0;
+    (&s.mass[0][0])[k] = 0ull;
   }
   __syncthreads();
   // Runs of one digit are merged in registers before they reach shared memory.
   uint32_t run_d = 0xffffffffu;
   unsigned run_n = 0;
-  double run_m = 0.0;
+  unsigned long long run_m = 0ull;
   float vmax = -INFINITY;
   auto flush = [&]() {
     if (run_n) {
@@ -217,10 +222,10 @@ __device__ void histogram(FtSmem& s, const Src& src, int shift, uint32_t prefix,
       flush();
       run_d = d;
       run_n = 0;
-      run_m = 0.0;
+      run_m = 0ull;
     }
     ++run_n;
-    if (by_mass) run_m += (double)exp2f(fmaf(v, c, -mc));
+    if (by_mass) run_m += __float2ull_rn(exp2f(fmaf(v, c, -mc)) * 0x1p44f);
   });
   flush();
   if (track_max) {
@@ -236,7 +241,9 @@ __device__ void histogram(FtSmem& s, const Src& src, int shift, uint32_t prefix,
   s.tc[tid] = tc;
   if (by_mass) {
     double tm = 0.0;
-    for (int w = 0; w < kHistCopies; ++w) tm += s.mass[w][tid];
+    unsigned long long tq = 0ull;
+    for (int w = 0; w < kHistCopies; ++w) tq += s.mass[w][tid];
+    tm = (double)tq * 0x1p-44;
     s.tm[tid] = tm;
   }
   if (tid == 0 && track_max) {
