@@ -65,6 +65,15 @@ __device__ __forceinline__ float value32(uint32_t k) {
 constexpr int kCand = 4096;      // logits that shared memory holds once few keys are left in play
 constexpr int kStreamK = 256;    // top-k up to this collects its candidates in one pass
 constexpr int kChunkWords = 4;   // 16-byte words a thread holds per chunk of the one-pass collection
+// Chunks between checkpoints of the one-pass collection. Top-p alone and
+// small top-k append few logits per chunk, so their checkpoints (barriers)
+// can be sparse; a large k fills the buffer faster and needs its floor
+// raised sooner. Measured on the benchmark batch: every 8 chunks for top-p
+// alone and k = 50, every 2 for k = 256 (every 8 there overflows the buffer
+// into the passes over the row).
+constexpr int kCheckSparse = 8;
+constexpr int kCheckDense = 2;
+constexpr int kSparseMaxK = 64;
 #ifndef SV_KTH_CHUNKS
 #define SV_KTH_CHUNKS 0x808Bu
 #endif
@@ -672,11 +681,12 @@ __device__ __forceinline__ bool stream_step(FtSmem& s, int V, int k, float p, fl
     }
   }
   if (cmax >= st.fl) append_chunk<DT>(s, cur, c, V, st, st.my_end, st.my_ovf);
-  // Checkpoints after every second chunk (and the last): the buffer's fill,
-  // the floor raise and the top-p bound. Between them a chunk appends at
-  // most CH logits, and an append that finds the buffer full is caught here.
-  if (!(c & 1) && c + 1 < nch) return true;
-  const int slot = ((c >> 1) + 1) & 1;  // chunk 0's own bound used slot 0
+  // Checkpoints after every `every` chunks (and the last): the buffer's
+  // fill, the floor raise and the top-p bound. An append between them that
+  // finds the buffer full is caught here.
+  const int every = k <= kSparseMaxK ? kCheckSparse : kCheckDense;  // k = 0: top-p alone
+  if ((c + 1) % every != 0 && c + 1 < nch) return true;
+  const int slot = (c / every + 1) & 1;  // chunk 0's own bound used slot 0
   if (k == 0 && c > 0) {
     float r = st.ref, sm = st.sum_all;
     warp_ref_mass(r, sm);
