@@ -3,7 +3,8 @@
  * verify-and-commit library (libspecverify.so).
  *
  * What the library computes is the verify-and-commit step of speculative
- * decoding and the model-free n-gram proposer, as these pages define them:
+ * decoding and the model-free proposers (n-gram and suffix), as these pages
+ * define them:
  *
  *   "Draft Model（草稿模型）" (compassingai.com), §2 "接受-拒绝准则" and the
  *   box "算法：Speculative Decoding (一步)": for draft slots i = 1..K in
@@ -23,7 +24,8 @@
  *
  *   "5.2 Draft 模型与无模型方案：怎样便宜地猜得更准", §4 "N-gram" and §6
  *   "动手实验": the prompt-lookup proposer; §4.3: a copied proposal is the
- *   one-hot distribution q(y) = 1 on the proposed token.
+ *   one-hot distribution q(y) = 1 on the proposed token; §5 "Suffix
+ *   Decoding": continuations ranked by how often they follow a suffix.
  *
  * Conventions for every entry point:
  *   - Array arguments are DEVICE pointers owned by the caller. The library
