@@ -202,13 +202,31 @@ struct CandSrc {
 // masses 2^(v c - mc) when by_mass; with track_max also the largest value
 // (into s.rowmax). Per-digit totals land in s.tc / s.tm, the mass total in
 // s.total_m.
-template <int DT, class Src>
+// kWarpBins: one bin copy per warp, kept in the one-pass collection's ring
+// (idle outside it), for mass passes over a whole row: a flat row's keys
+// crowd into few digits, and warps sharing bins serialize on their 64-bit
+// atomics. Otherwise the kHistCopies copies in FtSmem (cheaper to clear and
+// sum; enough for count passes and for the buffered candidates).
+template <int DT, class Src, bool kWarpBins = false>
 __device__ void histogram(FtSmem& s, const Src& src, int shift, uint32_t prefix, bool top_level,
                           uint32_t floor, bool by_mass, float c, float mc, bool track_max) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int k = tid; k < kHistCopies * 256; k += kFtThreads) {
-    (&s.cnt[0][0])[k] = 0u;
-    (&s.mass[0][0])[k] = 0ull;
+  constexpr int ncp = kWarpBins ? kFtWarps : kHistCopies;
+  static_assert(!kWarpBins || kFtWarps * 256 * (sizeof(unsigned) + sizeof(unsigned long long)) <= sizeof(s.ring),
+                "the per-warp bins fit in the ring");
+  unsigned* cnt;
+  unsigned long long* mass;
+  if constexpr (kWarpBins) {
+    cnt = reinterpret_cast<unsigned*>(&s.ring[0][0][0]);
+    mass = reinterpret_cast<unsigned long long*>(cnt + kFtWarps * 256);
+  } else {
+    cnt = &s.cnt[0][0];
+    mass = &s.mass[0][0];
+  }
+  const int cp = (kWarpBins ? warp : (warp & (kHistCopies - 1))) * 256;
+  for (int k = tid; k < ncp * 256; k += kFtThreads) {
+    cnt[k] = 0u;
+    mass[k] = 0ull;
   }
   __syncthreads();
   // Runs of one digit are merged in registers before they reach shared memory.
@@ -218,8 +236,8 @@ __device__ void histogram(FtSmem& s, const Src& src, int shift, uint32_t prefix,
   float vmax = -INFINITY;
   auto flush = [&]() {
     if (run_n) {
-      atomicAdd(&s.cnt[warp & (kHistCopies - 1)][run_d], run_n);
-      if (by_mass) atomicAdd(&s.mass[warp & (kHistCopies - 1)][run_d], run_m);
+      atomicAdd(&cnt[cp + run_d], run_n);
+      if (by_mass) atomicAdd(&mass[cp + run_d], run_m);
     }
   };
   src.each([&](uint32_t key, float v) {
@@ -246,12 +264,14 @@ __device__ void histogram(FtSmem& s, const Src& src, int shift, uint32_t prefix,
   // Counts stay integers; only mass levels pay for double precision (the
   // FP64 pipe is narrow on this part).
   unsigned tc = 0u;
-  for (int w = 0; w < kHistCopies; ++w) tc += s.cnt[w][tid];
+#pragma unroll
+  for (int w = 0; w < ncp; ++w) tc += cnt[w * 256 + tid];
   s.tc[tid] = tc;
   if (by_mass) {
     double tm = 0.0;
     unsigned long long tq = 0ull;
-    for (int w = 0; w < kHistCopies; ++w) tq += s.mass[w][tid];
+#pragma unroll
+    for (int w = 0; w < ncp; ++w) tq += mass[w * 256 + tid];
     tm = (double)tq * 0x1p-44;
     s.tm[tid] = tm;
   }
@@ -845,7 +865,7 @@ __device__ float row_threshold(FtSmem& s, const void* rowp, int V, bool vec, int
       if (in_smem)
         histogram<DT>(s, cs, sh, prefix, top, floor, true, c, mc, false);
       else
-        histogram<DT>(s, row, sh, prefix, top, floor, true, c, mc, false);
+        histogram<DT, RowSrc<DT>, true>(s, row, sh, prefix, top, floor, true, c, mc, false);
       // The buffer of the one-pass top-p holds only the logits near the
       // top: the mass the pass left out of it is added to the buffer's.
       if (top) need = (double)top_p * (mass_known ? s.total_m + s.row_mass : s.total_m);
