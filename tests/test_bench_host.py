@@ -57,3 +57,24 @@ def test_missing_power_counts_as_loaded_and_empty_file_gives_none():
     assert _summary(["not a sample"]) is None
     cs = bench.ClockSampler("0")           # nvidia-smi could not be started
     assert cs.summary() is None
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` times the oracle on the host cores (the
+    reference arm) and prints one JSON line with the arm's keys; it needs no
+    GPU."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "1", "--ref-budget-s", "1"],
+                         capture_output=True, text=True, check=True, timeout=600).stdout
+    d = json.loads(out.strip().splitlines()[-1])
+    assert d["impl"] == "reference" and d["unit"] == "rows/s" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["steps"] == 1 and d["n_gpus"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["metric"] == bench.METRIC and d["config"]["workload"] == bench.WORKLOAD
