@@ -124,3 +124,23 @@ def test_one_pass_collection_edges(cuda_lib, dtype, shape, top_k, top_p):
         b.target, b.draft = zt, zd.astype(np.float32)
     rep = _run(b, top_k, top_p)
     assert rep.mismatched_requests <= 1
+
+
+@pytest.mark.parametrize("top_k,top_p", [(50, 0.9), (0, 0.9)])
+def test_filtered_rerun_is_bit_identical(cuda_lib, top_k, top_p):
+    """The threshold kernel appends candidates in whatever order the atomics
+    give, but its counts and fixed-point mass sums are exact, so a repeated
+    call returns the same tokens, lengths and probabilities bit for bit (on
+    peaked rows, and on flat rows that take the passes over the row)."""
+    for b in (W.config3(seed=550, B=16),
+              W.gaussian_sampling(seed=551, B=16, K=5, V=60000, sigma=2.0, draft_sigma=0.75, T=1.0,
+                                  dtype="bf16")):
+        db = parity.to_device(b)
+        runs = []
+        for _ in range(3):
+            tok, ln, pr = api.spec_verify_filtered(db.target, db.draft, db.draft_tokens, db.cu_draft,
+                                                   db.uniforms, db.temperature, top_k, top_p, db.mode)
+            torch.cuda.synchronize()
+            runs.append((tok.clone(), ln.clone(), pr.clone()))
+        for r in runs[1:]:
+            assert all(torch.equal(x, y) for x, y in zip(runs[0], r))
