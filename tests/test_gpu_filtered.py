@@ -11,7 +11,7 @@ from speculative_decoding_verification_27_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _run(batch, top_k, top_p):
+def _run(batch, top_k, top_p, flag_budget=None):
     import oracle
     db = parity.to_device(batch)
     tok, ln, pr = api.spec_verify_filtered(db.target, db.draft, db.draft_tokens, db.cu_draft, db.uniforms,
@@ -19,7 +19,26 @@ def _run(batch, top_k, top_p):
     torch.cuda.synchronize()
     ora = oracle.spec_verify(batch.target, batch.draft, batch.draft_tokens, batch.cu_draft, batch.uniforms,
                              batch.temperature, batch.mode, top_k=top_k, top_p=top_p)
-    return parity.compare(batch, (tok.cpu().numpy(), ln.cpu().numpy(), pr.cpu().numpy()), ora)
+    return parity.compare(batch, (tok.cpu().numpy(), ln.cpu().numpy(), pr.cpu().numpy()), ora,
+                          flag_budget=flag_budget)
+
+
+def _proposals_from_filtered_draft(batch, top_k, top_p, seed):
+    """x̂ ~ q', the filtered draft distribution, as a draft model sampling
+    under the same filter proposes (the case in which the filtered step is
+    lossless). q' comes from the oracle; a proposal outside q' would be
+    rejected with certainty and leave an empty residual when p' = q'."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    u = np.random.default_rng(seed).random(batch.R_d)
+
+    def one(j):
+        q, _ = oracle.filtered_softmax(batch.draft[j], batch.temperature, top_k, top_p)
+        c = np.cumsum(q)
+        return min(int(np.searchsorted(c, u[j] * c[-1], side="right")), q.shape[0] - 1)
+    with ThreadPoolExecutor(max_workers=oracle.default_threads()) as ex:
+        return np.array(list(ex.map(one, range(batch.R_d))), np.int32)
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
@@ -42,6 +61,17 @@ def test_filtered_large_vocab_peaked_rows(cuda_lib, top_k, top_p):
     rep = _run(b, top_k, top_p)
     print(rep.as_dict())
     assert rep.mismatched_requests <= 1
+
+
+def test_filtered_config3_full_batch(cuda_lib):
+    """The benchmark batch (B=256, K=7, V=151936 bf16, T=0.7, peaked rows)
+    under top-k 50 / top-p 0.9, every request, proposals drawn from the
+    filtered draft; flagged rows within the 1e-4 budget."""
+    b = W.config3(seed=515)
+    b.draft_tokens = _proposals_from_filtered_draft(b, 50, 0.9, seed=516)
+    rep = _run(b, 50, 0.9, flag_budget=parity.FLAG_BUDGET)
+    print("filtered config3:", rep.as_dict())
+    assert rep.mismatched_requests <= 1e-4 * rep.rows
 
 
 def test_filtered_one_hot_and_ties(cuda_lib):
