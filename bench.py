@@ -323,18 +323,28 @@ def run_ours(args):
         e2e = {"value": R_t * world / (e_ms * 1e-3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms, "steps": n_e2e}
 
-    # CPU baseline and a live parity spot check on the same sample (rank 0, N=1).
+    # CPU baseline (rank 0, N=1): the oracle's own work on the step's batch,
+    # outputs only, timed over a few calls on all host threads. Then, untimed,
+    # a parity spot check: the oracle with its per-row probabilities against
+    # the GPU's outputs of the last timed step.
     cpu = None
     spot = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample = oracle_sample(batch, args.cpu_requests)
-        dt, threads, res = time_oracle(sample, diagnostics=True)
+        sample = batch if args.cpu_requests >= B else oracle_sample(batch, args.cpu_requests)
+        times = []
+        for _ in range(args.cpu_reps):
+            dt, threads, _ = time_oracle(sample, diagnostics=False)
+            times.append(dt)
+        dt = float(np.mean(times))
         cpu = {"value": sample.R_t / dt, "unit": "rows/s", "cores": threads, "kind": "oracle",
-               "sample": f"first {args.cpu_requests} of the 256 requests ({sample.R_t} target rows, "
-                         f"{sample.R_d} draft rows), one call, all host threads"}
+               "sample": (f"{'the whole batch' if sample.B == B else f'first {sample.B} of {B} requests'} "
+                          f"({sample.R_t} target rows, {sample.R_d} draft rows), {args.cpu_reps} calls, "
+                          "all host threads, the step's outputs only")}
+        _, _, res = time_oracle(sample, diagnostics=True)
         rt = sample.R_t
         g_tok, g_len, g_pr = out_tokens.cpu().numpy(), lens, out_probs.cpu().numpy()
-        rep = parity.compare(sample, (g_tok[:rt], g_len[:args.cpu_requests], g_pr[:rt]), res)
+        rep = parity.compare(sample, (g_tok[:rt], g_len[:sample.B], g_pr[:rt]), res,
+                             flag_budget=parity.FLAG_BUDGET)
         spot = rep.as_dict()
 
     if rank != 0:
@@ -537,19 +547,26 @@ def _extra_setup(name, seed):
             for f in ("target", "draft", "draft_tokens", "cu_draft", "uniforms") if getattr(d0, f) is not None}
     sample = b0 if b0.B <= 64 else oracle_sample(b0, 64)
 
+    def oracle_run(diagnostics):
+        if filtered:
+            import oracle
+            threads = min(oracle.default_threads(), sample.B)
+            res = oracle.spec_verify(sample.target, sample.draft, sample.draft_tokens, sample.cu_draft,
+                                     sample.uniforms, sample.temperature, sample.mode, threads,
+                                     diagnostics=diagnostics, top_k=FILTER_K, top_p=FILTER_P)
+            return threads, res
+        _, threads, res = time_oracle(sample, diagnostics=diagnostics)
+        return threads, res
+
     def oracle_fn():
-        reps = 200 if name == "verify_b1" else 1
+        # Timed: the step's outputs only. Untimed: the run with per-row
+        # probabilities that the spot check compares.
+        reps = 200 if name == "verify_b1" else 3
         t = time.perf_counter()
         for _ in range(reps):
-            if filtered:
-                import oracle
-                threads = min(oracle.default_threads(), sample.B)
-                res = oracle.spec_verify(sample.target, sample.draft, sample.draft_tokens, sample.cu_draft,
-                                         sample.uniforms, sample.temperature, sample.mode, threads,
-                                         top_k=FILTER_K, top_p=FILTER_P)
-            else:
-                _, threads, res = time_oracle(sample, diagnostics=True)
-        return (time.perf_counter() - t) / reps, threads, res
+            threads, _ = oracle_run(False)
+        dt = (time.perf_counter() - t) / reps
+        return dt, threads, oracle_run(True)[1]
 
     def check(res):
         k[0] = 0
@@ -675,7 +692,9 @@ def main():
     ap.add_argument("--batch", type=int, default=256,
                     help="requests per step (256 is the benchmark workload; smaller only for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-requests", type=int, default=64)
+    ap.add_argument("--cpu-requests", type=int, default=256,
+                    help="requests of the batch the CPU baseline times (default: all)")
+    ap.add_argument("--cpu-reps", type=int, default=3)
     ap.add_argument("--ref-budget-s", type=float, default=100.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -113,6 +113,45 @@ def new_workspace(B: int, R_t: int, V: int, device="cuda") -> torch.Tensor:
     return torch.zeros(spec_verify_workspace_size(B, R_t, V), dtype=torch.uint8, device=device)
 
 
+# Default workspaces, one per (device, stream, entry point): calls on one
+# stream run in order and the library leaves its counters at zero after each
+# call, so one block serves every call whose workspace layout is the same.
+# The layout follows (B, V) for spec_verify / spec_verify_greedy and (B, R_t,
+# V) for spec_verify_filtered (its thresholds come first); when it changes,
+# or the block is too small, the block is cleared (or grown to the next power
+# of two and cleared) before the call. Calls with an unchanged layout clear
+# nothing and allocate nothing.
+_default_ws: dict = {}
+
+
+def default_workspace(nbytes: int, device, stream=None, layout=None) -> torch.Tensor:
+    """The cached workspace of `stream` (current stream if None) on `device`
+    for calls with workspace layout `layout`, at least `nbytes` long. Calls
+    that pass no workspace use it; pass it to sv_check_status to read the
+    data-error bits of those calls."""
+    dev = torch.device(device)
+    idx = dev.index if dev.index is not None else torch.cuda.current_device()
+    s = torch.cuda.current_stream(idx) if stream is None else stream
+    key = (idx, s.cuda_stream, layout[0] if layout else None)
+    ent = _default_ws.get(key)
+    if ent is None or ent[0].numel() < nbytes:
+        size = 1 << max(12, (int(nbytes) - 1).bit_length())
+        with torch.cuda.stream(s):
+            ent = [torch.zeros(size, dtype=torch.uint8, device=torch.device("cuda", idx)), layout]
+        _default_ws[key] = ent
+    elif ent[1] != layout:
+        with torch.cuda.stream(s):
+            ent[0].zero_()
+        ent[1] = layout
+    return ent[0]
+
+
+def reset_default_workspaces() -> None:
+    """Drops the cached workspaces (needed only after SV_DEV_COPY_TIMEOUT,
+    which leaves a workspace's counters set)."""
+    _default_ws.clear()
+
+
 def spec_verify(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor,
                 cu_draft: torch.Tensor, uniforms: torch.Tensor, temperature: float,
                 mode: Optional[torch.Tensor] = None, *, out_tokens=None, out_len=None,
@@ -129,7 +168,8 @@ def spec_verify(target: torch.Tensor, draft: Optional[torch.Tensor], draft_token
     if out_probs is None and want_probs:
         out_probs = torch.empty((R_t, 2), dtype=torch.float32, device=dev)
     if workspace is None:
-        workspace = new_workspace(B, R_t, target.shape[1], dev)
+        workspace = default_workspace(spec_verify_workspace_size(B, R_t, target.shape[1]), dev, stream,
+                                      ("verify", B, target.shape[1]))
     st = lib.spec_verify(_ptr(target), _ptr(draft), _dtype(target), int(target.shape[1]), int(B),
                          _ptr(draft_tokens), _ptr(cu_draft), _ptr(mode), _ptr(uniforms),
                          float(temperature), _ptr(out_tokens), _ptr(out_len), _ptr(out_probs),
@@ -157,8 +197,14 @@ def spec_verify_noalloc(target: torch.Tensor, draft: Optional[torch.Tensor], dra
                         out_probs: Optional[torch.Tensor] = None,
                         status_out: Optional[torch.Tensor] = None, stream=None):
     """spec_verify on the library's fixed scratch block: no workspace argument
-    and no allocation. Outputs (and the optional one-element int32 status
-    tensor) are the caller's. Calls on one device must not overlap."""
+    and no allocation. Outputs are the caller's. Calls on one device must not
+    overlap.
+
+    status_out: a one-element int32 CUDA tensor that receives the call's
+    SV_DATA_* / SV_DEV_* bits (0 = clean). With None the bits are dropped:
+    a call with bad device data (offsets, tokens) then raises nothing and its
+    outputs are unspecified, and the block's own status word cannot be read
+    afterwards. Pass one whenever the inputs are not known to be valid."""
     B = cu_draft.shape[0] - 1
     st = _noalloc_fn()(_ptr(target), _ptr(draft), _dtype(target), int(target.shape[1]), int(B),
                        _ptr(draft_tokens), _ptr(cu_draft), _ptr(mode), _ptr(uniforms),
@@ -180,7 +226,8 @@ def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, cu_draf
     if out_len is None:
         out_len = torch.zeros(B, dtype=torch.int32, device=dev)
     if workspace is None:
-        workspace = new_workspace(B, R_t, target.shape[1], dev)
+        workspace = default_workspace(spec_verify_workspace_size(B, R_t, target.shape[1]), dev, stream,
+                                      ("verify", B, target.shape[1]))
     st = lib.spec_verify_greedy(_ptr(target), _dtype(target), int(target.shape[1]), int(B),
                                 _ptr(draft_tokens), _ptr(cu_draft), _ptr(out_tokens), _ptr(out_len),
                                 _ptr(workspace), workspace.numel(), _stream(stream))
@@ -361,7 +408,8 @@ def spec_verify_filtered(target: torch.Tensor, draft: Optional[torch.Tensor], dr
     if out_probs is None and want_probs:
         out_probs = torch.empty((R_t, 2), dtype=torch.float32, device=dev)
     if workspace is None:
-        workspace = torch.zeros(spec_verify_filtered_workspace_size(B, R_t, V), dtype=torch.uint8, device=dev)
+        workspace = default_workspace(spec_verify_filtered_workspace_size(B, R_t, V), dev, stream,
+                                      ("filtered", B, R_t, V))
     st = fn(_ptr(target), _ptr(draft), _dtype(target), int(V), int(B), int(R_t), _ptr(draft_tokens),
             _ptr(cu_draft), _ptr(mode), _ptr(uniforms), float(temperature), int(top_k), float(top_p),
             _ptr(out_tokens), _ptr(out_len), _ptr(out_probs), _ptr(workspace), workspace.numel(),

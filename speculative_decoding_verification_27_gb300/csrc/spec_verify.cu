@@ -1850,6 +1850,29 @@ static cudaError_t launch(const Params& P, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// The host checks of every verify entry point except those of the
+// workspace; makes no CUDA call. B == 0 passes (the call is then a no-op).
+static sv_status check_verify_args(const void* target, const void* draft, sv_dtype dtype, int32_t V,
+                                   int32_t B, const int32_t* draft_tokens, const int32_t* cu_draft,
+                                   const float* uniforms, float temperature, const int32_t* out_tokens,
+                                   const int32_t* out_len, const float* out_probs, int greedy_all) {
+  if (dtype != SV_FP32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+  if (B < 0 || V < 1 || V > max_vocab(dtype)) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!target || !cu_draft || !out_tokens || !out_len) return SV_ERR_INVALID_ARG;
+  if (!greedy_all) {
+    if (!uniforms) return SV_ERR_INVALID_ARG;
+    if (!(temperature > 0.f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
+  }
+  const size_t es = dtype == SV_FP32 ? 4 : 2;
+  if ((uintptr_t)target % es || (draft && (uintptr_t)draft % es)) return SV_ERR_INVALID_ARG;
+  if ((uintptr_t)cu_draft % 4 || (uintptr_t)out_tokens % 4 || (uintptr_t)out_len % 4 ||
+      (out_probs && (uintptr_t)out_probs % 4) || (uniforms && (uintptr_t)uniforms % 4) ||
+      (draft_tokens && (uintptr_t)draft_tokens % 4))
+    return SV_ERR_INVALID_ARG;
+  return SV_OK;
+}
+
 static sv_status run_verify(const void* target, const void* draft, sv_dtype dtype, int32_t V,
                             int32_t B, const int32_t* draft_tokens, const int32_t* cu_draft,
                             const uint8_t* mode, const float* uniforms, float temperature,
@@ -1857,20 +1880,11 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
                             void* workspace, size_t workspace_bytes, void* stream,
                             int greedy_all, const float* thr = nullptr,
                             const float* thr_d = nullptr) {
-  if (dtype != SV_FP32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
-  if (B < 0 || V < 1 || V > max_vocab(dtype)) return SV_ERR_INVALID_ARG;
-  if (B == 0) return SV_OK;
-  if (!target || !cu_draft || !out_tokens || !out_len || !workspace) return SV_ERR_INVALID_ARG;
-  if (!greedy_all) {
-    if (!uniforms) return SV_ERR_INVALID_ARG;
-    if (!(temperature > 0.f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
-  }
+  const sv_status chk = check_verify_args(target, draft, dtype, V, B, draft_tokens, cu_draft, uniforms,
+                                          temperature, out_tokens, out_len, out_probs, greedy_all);
+  if (chk != SV_OK || B == 0) return chk;
+  if (!workspace || (uintptr_t)workspace % 16) return SV_ERR_INVALID_ARG;
   const size_t es = dtype == SV_FP32 ? 4 : 2;
-  if ((uintptr_t)target % es || (draft && (uintptr_t)draft % es)) return SV_ERR_INVALID_ARG;
-  if ((uintptr_t)workspace % 16 || (uintptr_t)cu_draft % 4 || (uintptr_t)out_tokens % 4 ||
-      (uintptr_t)out_len % 4 || (out_probs && (uintptr_t)out_probs % 4) ||
-      (uniforms && (uintptr_t)uniforms % 4) || (draft_tokens && (uintptr_t)draft_tokens % 4))
-    return SV_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(B, V);
   if (workspace_bytes < L.rows + sizeof(RowRec)) return SV_ERR_INVALID_ARG;
 
@@ -1954,9 +1968,13 @@ sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logit
                               const float* uniforms, float temperature, int32_t* out_tokens,
                               int32_t* out_len, float* out_probs, uint32_t* status_out,
                               void* cuda_stream) {
-  if (B < 0 || V < 1 || (status_out && (uintptr_t)status_out % 4)) return SV_ERR_INVALID_ARG;
-  if (B == 0) return SV_OK;
-  if (!cu_draft) return SV_ERR_INVALID_ARG;
+  // Every host check comes before the first CUDA call, so a rejected call
+  // enqueues nothing (not even the clearing of the block).
+  if (status_out && (uintptr_t)status_out % 4) return SV_ERR_INVALID_ARG;
+  const sv_status chk = sv::check_verify_args(target_logits, draft_logits, dtype, V, B, draft_tokens,
+                                              cu_draft, uniforms, temperature, out_tokens, out_len,
+                                              out_probs, 0);
+  if (chk != SV_OK || B == 0) return chk;
   // The row count lives on the device; size the check by the largest R_t the
   // block could hold for this B and V, and let the kernel flag offsets past it.
   const sv::WsLayout L = sv::ws_layout(B, V);

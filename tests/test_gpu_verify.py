@@ -267,3 +267,40 @@ def test_ngram_long_history_read_from_global(cuda_lib):
     g = out.cpu().numpy()
     for b in range(B):
         assert np.array_equal(g[b, :o_cnt[b]], o_out[b, :o_cnt[b]])
+
+
+# --------------------------------------------------------------------------
+# The binding's default workspace
+# --------------------------------------------------------------------------
+def test_default_workspace_is_reused_without_clearing(cuda_lib):
+    """Calls that pass no workspace share one cached block per stream: after
+    the first call of a layout, a call launches the verify kernel alone (no
+    allocation, no fill); a new layout clears the block once; results stay
+    equal to the oracle's throughout."""
+    from torch.profiler import ProfilerActivity, profile
+    a = W.gaussian_sampling(seed=320, B=24, K=4, V=5000, sigma=2.0, draft_sigma=0.7, T=0.9, dtype="bf16")
+    c = W.gaussian_sampling(seed=321, B=40, K=3, V=5000, sigma=2.0, draft_sigma=0.7, T=0.9, dtype="bf16")
+    da, dc = parity.to_device(a), parity.to_device(c)
+    out = (torch.empty(max(a.R_t, c.R_t), dtype=torch.int32, device="cuda"),
+           torch.empty(max(a.B, c.B), dtype=torch.int32, device="cuda"),
+           torch.empty((max(a.R_t, c.R_t), 2), dtype=torch.float32, device="cuda"))
+
+    def call(b, db):
+        n = b.R_t
+        api.spec_verify(db.target, db.draft, db.draft_tokens, db.cu_draft, db.uniforms, db.temperature,
+                        db.mode, out_tokens=out[0][:n], out_len=out[1][:b.B], out_probs=out[2][:n])
+        torch.cuda.synchronize()
+        parity.compare(b, (out[0][:n].cpu().numpy(), out[1][:b.B].cpu().numpy(), out[2][:n].cpu().numpy()),
+                       parity.oracle_verify(b))
+
+    call(a, da)   # first call of this layout: the block is made and cleared
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        for _ in range(3):
+            call(a, da)
+    kernels = [e.key for e in prof.key_averages() if e.device_type.name == "CUDA" and "Memcpy" not in e.key]
+    assert kernels and all("verify_kernel" in k for k in kernels), kernels
+    call(c, dc)   # another B: cleared once, then reused
+    call(c, dc)
+    call(a, da)
+    ws = api.default_workspace(0, "cuda", layout=("verify", a.B, a.V))
+    assert api.sv_check_status(ws) == 0
