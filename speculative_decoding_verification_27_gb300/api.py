@@ -122,6 +122,7 @@ def new_workspace(B: int, R_t: int, V: int, device="cuda") -> torch.Tensor:
 # of two and cleared) before the call. Calls with an unchanged layout clear
 # nothing and allocate nothing.
 _default_ws: dict = {}
+default_workspace_clears = 0   # blocks allocated or cleared so far (each one fill launch)
 
 
 def default_workspace(nbytes: int, device, stream=None, layout=None) -> torch.Tensor:
@@ -132,14 +133,17 @@ def default_workspace(nbytes: int, device, stream=None, layout=None) -> torch.Te
     dev = torch.device(device)
     idx = dev.index if dev.index is not None else torch.cuda.current_device()
     s = torch.cuda.current_stream(idx) if stream is None else stream
+    global default_workspace_clears
     key = (idx, s.cuda_stream, layout[0] if layout else None)
     ent = _default_ws.get(key)
     if ent is None or ent[0].numel() < nbytes:
+        default_workspace_clears += 1
         size = 1 << max(12, (int(nbytes) - 1).bit_length())
         with torch.cuda.stream(s):
             ent = [torch.zeros(size, dtype=torch.uint8, device=torch.device("cuda", idx)), layout]
         _default_ws[key] = ent
     elif ent[1] != layout:
+        default_workspace_clears += 1
         with torch.cuda.stream(s):
             ent[0].zero_()
         ent[1] = layout
