@@ -41,8 +41,8 @@ WORKLOAD = ("sampling verify B=256 K=7 V=151936 bf16 T=0.7, peaked rank-score ro
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per verify launch on this workload from one ncu
 # capture, valid only for the kernel sources whose hash is recorded with it.
-TRAFFIC = {"sources_sha256": "f4d5bc4d6180888943d4e785458afb9b72700198f7f5611239e16be0933b7ed0",
-           "bytes_per_launch": 1235410000 + 4466432,
+TRAFFIC = {"sources_sha256": "1007868c993b0dfb0c790d500e8b8131450ccd99353df1dd31aacf3648e948be",
+           "bytes_per_launch": 1236024000 + 4343552,
            "profile": "profiles/verify_kernel_sampling_B256_K7_V151936_bf16.md"}
 
 

@@ -6,8 +6,7 @@
 //      out in request order by an atomic counter. The CTA streams the target
 //      row (and, for a sampled draft slot, the paired draft row) once through
 //      a ring of shared-memory stages filled by bulk asynchronous copies (the
-//      TMA engine), with bulk L2 prefetches running a few chunks ahead of the
-//      ring, and keeps a single-pass online softmax: per thread a running
+//      TMA engine), and keeps a single-pass online softmax: per thread a running
 //      maximum and one fp32 partial sum per vector lane, rescaled when the
 //      maximum grows. Sums are combined in double-float arithmetic, so
 //      S = sum_x 2^(z_x c - Mc) (c = log2(e)/T, Mc = fp32(max z * c)) is
@@ -26,9 +25,9 @@
 //        all accepted       r = p                  (bonus token, algorithm box)
 //        greedy request     the argmax of row s
 //      The draw is the inverse CDF in vocabulary order: the smallest k whose
-//      running sum of r exceeds u' * sum(r). The stop row (pair) is
-//      prefetched into L2 whole, then streamed through the ring once to sum
-//      r over every tile; only the tile that holds the target is rescanned.
+//      running sum of r exceeds u' * sum(r). The stop row (pair) is streamed
+//      through the ring once, last chunk first, to sum r over every tile;
+//      only the tile that holds the target is rescanned.
 //   The last CTA to leave resets the work counter, and each request's counter
 //   is reset by its commit, so the workspace is left zeroed.
 //
@@ -1528,21 +1527,24 @@ __device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const P
         // draft row or q = 1 for a one-hot proposal.
         const float zp = s.zx_ok ? s.zx_p : mask_below<DT>(Elem<DT & 1>::scalar(trow, xhat), s.tau_t);
         const float ap = fmaf(zp, P.c, -mcp);
-        const double pd = (double)exp2f(ap) / Sp;
-        double rho;
-        double qd = 1.0;
+        // In fp32: p(x̂), q(x̂) and rho come out to a few ulp (about 2e-7 at
+        // most), far inside the 1e-6 within which a decision counts as a tie
+        // with the float64 evaluation; fp64 divisions cost this step more on
+        // this part than the bytes it saves.
+        const float Spf = (float)Sp, Sqf = (float)Sq;
+        const float pd = __fdiv_rn(exp2f(ap), Spf);
+        float rho, qd = 1.f;
         if (has_d) {
           const float zq = s.zx_ok ? s.zx_q : mask_below<DT>(Elem<DT & 1>::scalar(drow, xhat), s.tau_d);
           const float aq = fmaf(zq, P.c, -mcq);
-          qd = (double)exp2f(aq) / Sq;
-          rho = (zq == -INFINITY) ? 0.0 : fmin(1.0, (double)exp2f(ap - aq) * (Sq / Sp));
+          qd = __fdiv_rn(exp2f(aq), Sqf);
+          rho = (zq == -INFINITY) ? 0.f : fminf(1.f, __fmul_rn(exp2f(ap - aq), __fdiv_rn(Sqf, Spf)));
         } else {
-          rho = fmin(1.0, pd);
+          rho = fminf(1.f, pd);
         }
-        const double u = (double)s.u_acc;
-        acc = (u < rho) ? 1u : 0u;
-        ph = (float)pd;
-        qh = (float)qd;
+        acc = (s.u_acc < rho) ? 1u : 0u;
+        ph = pd;
+        qh = qd;
       }
       rec.accept = acc;
       if (P.out_probs) {
