@@ -273,21 +273,42 @@ class AdaptiveDraftLength:
 # ---------------------------------------------------------------------------
 # Multi-candidate verification: keep the candidate with the longest commit
 # ---------------------------------------------------------------------------
-def select_candidates(cu_cand, out_len):
-    """Request b owns candidates cu_cand[b] .. cu_cand[b+1]-1 (each verified
-    as its own request, "投机解码从零实现" §5.1 批量验证: one pass verifies
-    several drafts, each returning its accepted tokens and gain). The kept
-    candidate is the one with the longest committed length, the lowest index
-    among ties. Returns (best [B] global candidate index, or -1 for a
-    request without candidates; best_len [B], 0 then)."""
+def select_candidates(cu_cand, out_len, policy: str = "uniform", u_select=None):
+    """Request b owns candidates cu_cand[b] .. cu_cand[b+1]-1, each verified as
+    its own request ("投机解码从零实现" §5.1 批量验证: one pass verifies several
+    drafts, each returning its accepted tokens and gain). The page does not
+    say which result to keep; two rules:
+
+    "uniform": candidate cu_cand[b] + min(n - 1, floor(u * n)) for n
+      candidates and the request's selection uniform u = u_select[b] (a
+      negative or NaN u picks the first). The choice does not depend on any
+      verification outcome, so the kept commit is distributed as a single
+      candidate's: lossless ("Draft Model（草稿模型）" §2).
+    "longest": the longest committed length, the lowest index among ties.
+      It raises the expected gain but looks at the outcomes, so the kept
+      commit is no longer distributed as the target's.
+
+    Returns (best [B] global candidate index, or -1 for a request without
+    candidates; best_len [B], 0 then)."""
     cu = [int(x) for x in cu_cand]
     lens = [int(x) for x in out_len]
+    if policy not in ("uniform", "longest"):
+        raise ValueError(policy)
+    if policy == "uniform" and u_select is None:
+        raise ValueError("the uniform rule needs u_select")
     best, best_len = [], []
     for b in range(len(cu) - 1):
+        n = cu[b + 1] - cu[b]
         bi, bl = -1, 0
-        for c in range(cu[b], cu[b + 1]):
-            if bi < 0 or lens[c] > bl:
-                bi, bl = c, lens[c]
+        if n > 0 and policy == "uniform":
+            u = float(u_select[b])
+            j = int(np.floor(u * n)) if u >= 0.0 else 0
+            bi = cu[b] + min(n - 1, j)
+            bl = lens[bi]
+        elif n > 0:
+            for c in range(cu[b], cu[b + 1]):
+                if bi < 0 or lens[c] > bl:
+                    bi, bl = c, lens[c]
         best.append(bi)
         best_len.append(bl)
     return np.array(best, np.int32), np.array(best_len, np.int32)

@@ -95,6 +95,18 @@ def uniforms_for(cu_draft: np.ndarray, seed: int, round_index: int = 0) -> np.nd
     return ((w[:, :2] >> np.uint32(8)).astype(np.float32) * np.float32(2.0 ** -24)).astype(np.float32)
 
 
+def selection_uniforms(B: int, seed: int, round_index: int = 0) -> np.ndarray:
+    """[B] float32 in [0, 1): one uniform per request for choosing among its
+    draft candidates, drawn apart from the verify uniforms: Philox counter
+    (b, 0, round, 1); u = (w0 >> 8) * 2^-24."""
+    ctr = np.zeros((int(B), 4), np.uint32)
+    ctr[:, 0] = np.arange(int(B), dtype=np.uint32)
+    ctr[:, 2] = round_index
+    ctr[:, 3] = 1
+    w = philox4x32_10(ctr, _seed_key(seed))
+    return ((w[:, 0] >> np.uint32(8)).astype(np.float32) * np.float32(2.0 ** -24)).astype(np.float32)
+
+
 # ----------------------------------------------------------------------------
 # bf16 storage
 # ----------------------------------------------------------------------------

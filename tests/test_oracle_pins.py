@@ -519,8 +519,64 @@ def test_filtered_verify_is_lossless_for_the_filtered_target(oracle_mod):
 def test_select_candidates_worked_example(oracle_mod):
     """Three requests: candidates (2, 5, 5) keep the first 5; (1) keeps it;
     none gives -1."""
-    best, best_len = oracle_mod.select_candidates([0, 3, 4, 4], [2, 5, 5, 1])
+    best, best_len = oracle_mod.select_candidates([0, 3, 4, 4], [2, 5, 5, 1], "longest")
     assert best.tolist() == [1, 3, -1] and best_len.tolist() == [5, 1, 0]
+
+
+def test_select_candidates_uniform_worked_example(oracle_mod):
+    """floor(u * n): u = 0.5 of 3 candidates keeps the second, u just below 1
+    the last, u = 0 the first; one candidate is always kept; a negative u
+    keeps the first."""
+    cu, lens = [0, 3, 4, 4, 6], [2, 5, 5, 1, 3, 4]
+    best, best_len = oracle_mod.select_candidates(cu, lens, "uniform", [0.5, 0.9, 0.3, 1 - 2 ** -24])
+    assert best.tolist() == [1, 3, -1, 5] and best_len.tolist() == [5, 1, 0, 4]
+    best, _ = oracle_mod.select_candidates(cu, lens, "uniform", [0.0, 0.0, 0.0, 0.0])
+    assert best.tolist() == [0, 3, -1, 4]
+    best, _ = oracle_mod.select_candidates(cu, lens, "uniform", [1 - 2 ** -24, -0.5, 0.5, 0.5])
+    assert best.tolist() == [2, 3, -1, 5]
+    # Each of n candidates is kept for exactly 1/n of the uniform's lattice.
+    n = 3
+    u = np.arange(0, 2 ** 24, 4099, dtype=np.float64) / 2 ** 24
+    picks = [oracle_mod.select_candidates([0, n], [1] * n, "uniform", [x])[0][0] for x in u]
+    frac = np.bincount(picks, minlength=n) / len(picks)
+    assert np.abs(frac - 1 / n).max() < 2e-3
+
+
+def _two_candidate_rounds(oracle_mod, N, seed):
+    """N requests of two candidates; each candidate proposes one token drawn
+    from q (K = 1) and is verified as its own request."""
+    rng = np.random.default_rng(seed)
+    V, T = 16, 1.0
+    zp = rng.normal(0, 1.5, V).astype(np.float32)
+    zb = rng.normal(0, 1.5, V).astype(np.float32)
+    zq = (zp + rng.normal(0, 1.0, V)).astype(np.float32)
+    p = sp_softmax(zp.astype(np.float64))
+    q = sp_softmax(zq.astype(np.float64))
+    C = 2 * N
+    cu = np.arange(C + 1, dtype=np.int32)
+    toks = _sample(q, C, rng)
+    r = oracle_mod.spec_verify(np.tile(np.stack([zp, zb]), (C, 1)), np.tile(zq[None], (C, 1)), toks, cu,
+                               W.uniforms_for(cu, seed=seed + 1), T, diagnostics=False)
+    cu_cand = np.arange(0, C + 1, 2, dtype=np.int32)
+    return p, r, cu_cand
+
+
+def test_select_uniform_is_lossless_and_longest_is_not(oracle_mod):
+    """Two candidates per request, each drawn from q and verified alone. The
+    uniform rule's kept first token follows p (chi-square, 15 dof); the
+    longest rule's, which prefers the candidate that was accepted, does not."""
+    N = 500_000
+    p, r, cu_cand = _two_candidate_rounds(oracle_mod, N, 31)
+    first = r.out_tokens.reshape(-1, 2)[:, 0]   # each candidate: target rows (slot 0, bonus)
+    u = W.selection_uniforms(N, seed=33)
+    for policy, lossless in (("uniform", True), ("longest", False)):
+        best, _ = oracle_mod.select_candidates(cu_cand, r.out_len, policy, u)
+        hist = np.bincount(first[best], minlength=16)
+        chi2 = float(((hist - N * p) ** 2 / (N * p)).sum())
+        if lossless:
+            assert chi2 < CHI2_15DOF_999, chi2
+        else:
+            assert chi2 > 50 * CHI2_15DOF_999, chi2
 
 
 # --------------------------------------------------------------------------

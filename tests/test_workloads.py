@@ -99,3 +99,14 @@ def test_config4_histories_coverage():
             grams[h[s:s + 8].tobytes()] += 1
         positions_in_copies = sum(c for c in grams.values() if c > 1)
         assert positions_in_copies > 0.3 * 2048  # copies and their sources
+
+
+def test_selection_uniforms_are_on_the_lattice_and_apart_from_the_verify_uniforms():
+    u = W.selection_uniforms(5000, seed=4)
+    assert u.dtype == np.float32 and np.all(u >= 0) and np.all(u < 1)
+    assert np.all((u * 2 ** 24) == np.floor(u * 2 ** 24))
+    cu = np.arange(5001, dtype=np.int32)
+    v = W.uniforms_for(cu, seed=4)
+    assert not np.any(u == v[::2, 0][:5000])
+    assert np.array_equal(u, W.selection_uniforms(5000, seed=4))
+    assert abs(float(u.mean()) - 0.5) < 0.02
