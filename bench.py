@@ -402,7 +402,7 @@ EXTRA_WORKLOADS = {
     "topkp_b256": "top-k 50 / top-p 0.9 filtered sampling verify on the benchmark batch (B=256 K=7 "
                   "V=151936 bf16 T=0.7, peaked rank-score rows)",
     "candidates_b64x4": "64 requests x 4 draft candidates of 5 tokens (V=32000 bf16, T=1.0), verified as "
-                        "256 requests, then the longest commit kept per request",
+                        "256 requests, then one kept per request by its selection uniform (lossless rule)",
 }
 FILTER_K, FILTER_P = 50, 0.9
 SUFFIX_SHARE, SUFFIX_OCC = 0.5, 256
@@ -519,6 +519,7 @@ def _extra_setup(name, seed):
     cands = name == "candidates_b64x4"
     if cands:
         cu_cand = torch.arange(0, 257, 4, dtype=torch.int32, device="cuda")
+        u_sel = torch.from_numpy(W.selection_uniforms(64, seed=seed)).cuda()
         best = torch.empty(64, dtype=torch.int32, device="cuda")
         best_len = torch.empty(64, dtype=torch.int32, device="cuda")
     if filtered:
@@ -540,7 +541,7 @@ def _extra_setup(name, seed):
                             db.temperature, db.mode, out_tokens=ot, out_len=ol, out_probs=op,
                             workspace=ws)
             if cands:
-                api.sv_select_candidates(cu_cand, ol, best=best, best_len=best_len)
+                api.sv_select_candidates(cu_cand, ol, api.SV_SELECT_UNIFORM, u_sel, best=best, best_len=best_len)
 
     d0 = dbs[0]
     host = {f: (getattr(d0, f), getattr(d0, f).cpu().pin_memory())

@@ -318,20 +318,34 @@ sv_status sv_pack_drafts(const int32_t* tokens, const int32_t* counts, int32_t B
 /*
  * Multi-candidate verification ("投机解码从零实现", §5.1 "批量验证": one
  * target pass verifies several draft candidates, each returning its
- * accepted tokens and gain). Flatten every request's candidates into one
- * spec_verify call, each candidate its own request; request b owns
- * candidates cu_cand[b] .. cu_cand[b+1]-1 of that call. This call then keeps
- * per request the candidate with the longest committed length (lowest index
- * among ties): best[b] is its index in the flattened call (-1 if the request
- * had no candidate) and best_len[b] its out_len (0 then). All pointers are
- * device arrays; asynchronous on `cuda_stream`.
+ * accepted tokens and gain; the page does not say which result to keep).
+ * Flatten every request's candidates into one spec_verify call, each
+ * candidate its own request; request b owns candidates cu_cand[b] ..
+ * cu_cand[b+1]-1 of that call. This call keeps one candidate per request:
+ * best[b] is its index in the flattened call (-1 if the request had no
+ * candidate) and best_len[b] its out_len (0 then). The rule is `policy`:
  *
- * Keeping the longest of independently verified candidates raises the
- * expected gain, but it does not preserve the target distribution: each
- * candidate alone is lossless, the choice among them is not.
+ *   SV_SELECT_UNIFORM: candidate min(n - 1, floor(u_select[b] * n)) of the
+ *     request's n candidates (a negative u picks the first). u_select [B]
+ *     float32 holds one uniform in [0, 1) per request, drawn independently
+ *     of the verify uniforms. The choice depends on no verification outcome,
+ *     so the kept commit is distributed exactly as a single candidate's: the
+ *     step stays lossless ("Draft Model（草稿模型）", §2). It does not raise
+ *     the expected number of committed tokens over one candidate.
+ *   SV_SELECT_LONGEST_BIASED: the longest committed length (lowest index
+ *     among ties); u_select may be NULL. This raises the expected gain but
+ *     looks at the outcomes: each candidate alone is lossless, the choice
+ *     among them is not, and the kept tokens no longer follow the target
+ *     distribution. Opt in knowingly.
+ *
+ * All pointers are device arrays; asynchronous on `cuda_stream`.
+ * SV_ERR_INVALID_ARG for an unknown policy, a missing u_select under
+ * SV_SELECT_UNIFORM, bad pointers or B < 0.
  */
+enum { SV_SELECT_UNIFORM = 0, SV_SELECT_LONGEST_BIASED = 1 };
 sv_status sv_select_candidates(const int32_t* cu_cand, const int32_t* out_len, int32_t B,
-                               int32_t* best, int32_t* best_len, void* cuda_stream);
+                               int32_t policy, const float* u_select, int32_t* best,
+                               int32_t* best_len, void* cuda_stream);
 
 /*
  * Acceptance statistics ("5.2 Draft 模型与无模型方案", §7.1 and §7.2),

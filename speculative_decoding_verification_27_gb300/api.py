@@ -422,19 +422,25 @@ def spec_verify_filtered(target: torch.Tensor, draft: Optional[torch.Tensor], dr
     return out_tokens, out_len, out_probs
 
 
-def sv_select_candidates(cu_cand: torch.Tensor, out_len: torch.Tensor, *, best=None, best_len=None,
+SV_SELECT_UNIFORM, SV_SELECT_LONGEST_BIASED = 0, 1
+
+
+def sv_select_candidates(cu_cand: torch.Tensor, out_len: torch.Tensor, policy: int,
+                         u_select: Optional[torch.Tensor] = None, *, best=None, best_len=None,
                          stream=None):
-    """Per request, the candidate with the longest commit. Returns (best, best_len)."""
+    """Per request, the kept candidate under `policy` (SV_SELECT_UNIFORM needs
+    one selection uniform per request in u_select; SV_SELECT_LONGEST_BIASED
+    is not distribution-preserving). Returns (best, best_len)."""
     lib = load()
     fn = lib.sv_select_candidates
     P = ctypes.c_void_p
-    fn.argtypes = [P, P, ctypes.c_int32, P, P, P]
+    fn.argtypes = [P, P, ctypes.c_int32, ctypes.c_int32, P, P, P, P]
     fn.restype = ctypes.c_int
     B = cu_cand.shape[0] - 1
     if best is None:
         best = torch.empty(B, dtype=torch.int32, device=cu_cand.device)
     if best_len is None:
         best_len = torch.empty(B, dtype=torch.int32, device=cu_cand.device)
-    _check("sv_select_candidates", fn(_ptr(cu_cand), _ptr(out_len), int(B), _ptr(best), _ptr(best_len),
-                                      _stream(stream)))
+    _check("sv_select_candidates", fn(_ptr(cu_cand), _ptr(out_len), int(B), int(policy), _ptr(u_select),
+                                      _ptr(best), _ptr(best_len), _stream(stream)))
     return best, best_len

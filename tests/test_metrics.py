@@ -107,7 +107,8 @@ def test_metrics_kernel_large_batch_and_clamping(cuda_lib, oracle_mod):
 
 
 @pytest.mark.gpu
-def test_select_candidates_after_a_flattened_verify(cuda_lib, oracle_mod):
+@pytest.mark.parametrize("policy", ["uniform", "longest"])
+def test_select_candidates_after_a_flattened_verify(cuda_lib, oracle_mod, policy):
     """Requests with 0..5 candidates, each candidate verified as its own
     request; the kept candidate matches the oracle's rule on the GPU's own
     lengths, and the flattened verify matches the oracle."""
@@ -119,12 +120,26 @@ def test_select_candidates_after_a_flattened_verify(cuda_lib, oracle_mod):
     C = int(cu_cand[-1])
     flat = W.gaussian_sampling(seed=71, B=C, K=rng.integers(1, 7, size=C).astype(np.int32), V=5000,
                                sigma=1.0, draft_sigma=0.3, T=1.0, dtype="bf16")
+    u = W.selection_uniforms(B, seed=72)
+    u[:3] = [0.0, 1 - 2 ** -24, -0.25]  # the ends of the range, and a negative u
     db = parity.to_device(flat)
     tok, ln, pr = api.spec_verify(db.target, db.draft, db.draft_tokens, db.cu_draft, db.uniforms,
                                   db.temperature)
-    best, best_len = api.sv_select_candidates(torch.from_numpy(cu_cand).cuda(), ln)
+    pol = api.SV_SELECT_UNIFORM if policy == "uniform" else api.SV_SELECT_LONGEST_BIASED
+    best, best_len = api.sv_select_candidates(torch.from_numpy(cu_cand).cuda(), ln, pol,
+                                              torch.from_numpy(u).cuda() if policy == "uniform" else None)
     torch.cuda.synchronize()
     parity.compare(flat, (tok.cpu().numpy(), ln.cpu().numpy(), pr.cpu().numpy()), parity.oracle_verify(flat))
-    want_b, want_l = oracle_mod.select_candidates(cu_cand, ln.cpu().numpy())
+    want_b, want_l = oracle_mod.select_candidates(cu_cand, ln.cpu().numpy(), policy, u)
     assert np.array_equal(best.cpu().numpy(), want_b) and np.array_equal(best_len.cpu().numpy(), want_l)
     assert (want_b == -1).sum() == (M == 0).sum()
+
+
+@pytest.mark.gpu
+def test_select_candidates_rejects_an_unknown_policy_or_a_missing_uniform(cuda_lib):
+    cu = torch.zeros(2, dtype=torch.int32, device="cuda")
+    ln = torch.ones(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(api.SpecVerifyError):
+        api.sv_select_candidates(cu, ln, 7)
+    with pytest.raises(api.SpecVerifyError):
+        api.sv_select_candidates(cu, ln, api.SV_SELECT_UNIFORM, None)
