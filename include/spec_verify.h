@@ -251,6 +251,78 @@ sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logit
                               void* cuda_stream);
 
 /*
+ * Vocabulary-sharded verify-and-commit: the step of spec_verify ("Draft
+ * Model（草稿模型）" §2) when each rank holds only a slice of the vocabulary,
+ * as a tensor-parallel LM head leaves it. The pages deploy the draft and the
+ * target on separate nodes ("Speculative Decoding在分布式推理中的应用" §三)
+ * but do not split the vocabulary; this form is the library's own, and the
+ * only split of the step that needs an exchange between GPUs. Shard s of S
+ * holds columns [v0_s, v0_s + Vs_s) of every target and draft row; the
+ * shards cover [0, V) in rank order. Per call,
+ * every rank runs, between two exchanges that the caller performs (the
+ * Python binding's spec_verify_vsharded does them with torch.distributed):
+ *
+ *   sv_vshard_stats    per row of its slice: mc = fp32(max z * c), the sum
+ *                      S of 2^(z c - mc) (c = log2(e)/T), the logit of the
+ *                      row's proposed token if the shard holds it, and the
+ *                      argmax (largest logit, lowest global index);
+ *   -- all-gather of the statistics: [S, R_t] (and [S, R_d]) in rank order --
+ *   sv_vshard_decide   every rank, identically: the whole-vocabulary p(x̂),
+ *                      q(x̂), the accept tests (as spec_verify), the stop
+ *                      slot, the accepted prefix, out_len, out_probs of the
+ *                      draft slots, greedy tokens, and one draw job per
+ *                      sampled request (in `jobs`, sv_vshard_jobs_bytes(B));
+ *   sv_vshard_masses   this shard's mass of the draw's r (max(0, p - q), p
+ *                      without the rejected one-hot proposal, or p) over its
+ *                      slice, per request, in units of 2^(z c - Mc_p);
+ *   -- all-gather of the masses: [S, B], an exclusive scan in shard order --
+ *   sv_vshard_draw     the shard whose part of the scan holds u' * Z
+ *                      (u' = uniforms[stop row, 1]) locates the token in its
+ *                      slice; the others give -1 (and probabilities -1);
+ *   -- element-wise max over the shards of draw_tok [B] and draw_prob [B, 2] --
+ *   sv_vshard_finish   writes the drawn tokens (and (p(y), q(y)) into the
+ *                      bonus rows of out_probs).
+ *
+ * Arguments as for spec_verify, plus: logits are the shard's [rows, ld]
+ * row-major slices (ld >= Vs elements); R_t = cu_draft[B] + B; status is a
+ * device uint32 that collects SV_DATA_* bits (clear it before the call).
+ * All pointers are device pointers; every call is asynchronous on its
+ * stream. Results equal spec_verify's up to the summation order of the
+ * shards (decisions within ~1e-6 of a tie can differ).
+ */
+typedef struct {
+  float mc;       /* fp32(max z * c) of the slice's row, 0 if it has no finite logit */
+  float zx;       /* logit of the row's proposed token, if has_x */
+  double S;       /* sum of 2^(z c - mc) over the slice's row */
+  float amax_v;   /* largest logit of the slice's row (-inf if none) */
+  int32_t amax_i; /* its lowest global index (INT32_MAX if none) */
+  int32_t has_x;  /* this shard holds the proposed token */
+  int32_t pad;
+} sv_shard_stat;
+size_t sv_vshard_jobs_bytes(int32_t B);
+sv_status sv_vshard_stats(const void* logits, sv_dtype dtype, int32_t rows, int32_t Vs, int64_t ld,
+                          int32_t v0, int32_t V, int32_t is_draft, int32_t B, const int32_t* cu_draft,
+                          const int32_t* draft_tokens, float temperature, sv_shard_stat* out,
+                          uint32_t* status, void* cuda_stream);
+sv_status sv_vshard_decide(const sv_shard_stat* target_stats, const sv_shard_stat* draft_stats,
+                           int32_t S, int32_t V, int32_t B, int32_t R_t, const int32_t* cu_draft,
+                           const int32_t* draft_tokens, const uint8_t* mode, const float* uniforms,
+                           float temperature, int32_t* out_tokens, int32_t* out_len, float* out_probs,
+                           void* jobs, uint32_t* status, void* cuda_stream);
+sv_status sv_vshard_masses(const void* target, const void* draft, sv_dtype dtype, int32_t Vs, int64_t ld,
+                           int32_t v0, int32_t B, int32_t R_t, const int32_t* cu_draft,
+                           const sv_shard_stat* target_stats, const void* jobs, float temperature,
+                           double* masses, void* cuda_stream);
+sv_status sv_vshard_draw(const void* target, const void* draft, sv_dtype dtype, int32_t Vs, int64_t ld,
+                         int32_t v0, int32_t shard, int32_t S, int32_t B, int32_t R_t,
+                         const int32_t* cu_draft, const double* masses, const sv_shard_stat* target_stats,
+                         const void* jobs, const float* uniforms, float temperature, int32_t* draw_tok,
+                         float* draw_prob, uint32_t* status, void* cuda_stream);
+sv_status sv_vshard_finish(const void* jobs, int32_t B, int32_t R_t, const int32_t* draw_tok,
+                           const float* draw_prob, int32_t* out_tokens, float* out_probs, uint32_t* status,
+                           void* cuda_stream);
+
+/*
  * N-gram / prompt-lookup proposer ("5.2 Draft 模型与无模型方案", §4.1 and §6):
  * for n = min(max_n, L) down to min_n, take the tail h[L-n, L) of the
  * history and find the most recent earlier start s, 0 <= s <= L-2n-1, with
