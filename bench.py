@@ -16,9 +16,12 @@ Prints one JSON line (rank 0):
              on the launching stream) against the measured copy bandwidth
   cpu_baseline  the float64 oracle on the host cores, on a bounded sample
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--strong]
 Under torchrun each rank runs its own batch on its own GPU (weak scaling; the
-requests are independent, so there is no data-path collective).
+requests are independent, so there is no data-path collective). With
+--strong the ranks split one global batch by requests (sharding.py, balanced
+by the logit rows each request reads) and, after the timed region, gather
+their outputs; rank 0 checks them against one verify of the whole batch.
 """
 from __future__ import annotations
 
@@ -235,7 +238,16 @@ def run_ours(args):
     build.build_library()
     api.load()
 
-    batch = make_batch(rank_seed(args.seed, rank), args.batch)
+    full = None
+    if args.strong:
+        # One global batch, the same on every rank; each verifies its share.
+        from speculative_decoding_verification_27_gb300 import sharding
+        full = make_batch(args.seed, args.batch)
+        bounds = sharding.partition_requests(full.cu_draft, world, full.greedy_mask(), full.draft is not None)
+        shard = sharding.shard_of(full.cu_draft, int(bounds[rank]), int(bounds[rank + 1]))
+        batch = sharding.local_batch(full, shard)
+    else:
+        batch = make_batch(rank_seed(args.seed, rank), args.batch)
     db = parity.to_device(batch)
     B, R_t = batch.B, batch.R_t
     ws = api.new_workspace(B, R_t, batch.V)
@@ -277,11 +289,39 @@ def run_ours(args):
     mean_launch_ms = float(np.mean(per_launch_ms))
 
     lens = out_len.cpu().numpy()
-    committed = int(lens.sum())
+    committed = int(lens.sum()) * world   # all ranks' batches have the same shape
+    mean_len = float(lens.sum()) / B
     K = np.diff(batch.cu_draft)
     accepted = int((lens - 1).sum())
     alg_bytes = batch.algorithmic_bytes()
     value = R_t * world / (ms_per_step * 1e-3)
+    strong = None
+    if args.strong:
+        # Strong scaling: the global batch's rows over the slowest rank's time;
+        # the shards' outputs gathered in rank order must equal one verify of
+        # the whole batch (rank 0 checks, on its own GPU, after the timing).
+        from speculative_decoding_verification_27_gb300 import sharding
+        g_tok, g_len, g_pr = out_tokens.cpu().numpy(), lens, out_probs.cpu().numpy()
+        if world > 1:
+            g_tok, g_len, g_pr = sharding.gather_outputs(g_tok, g_len, g_pr)
+        value = full.R_t / (ms_per_step * 1e-3)
+        committed = int(g_len.sum())
+        mean_len = committed / full.B
+        accepted = int((g_len - 1).sum())
+        K = np.diff(full.cu_draft)
+        if rank == 0:
+            dfull = parity.to_device(full)
+            w_tok, w_len, w_pr = api.spec_verify(dfull.target, dfull.draft, dfull.draft_tokens, dfull.cu_draft,
+                                                 dfull.uniforms, dfull.temperature, dfull.mode)
+            torch.cuda.synchronize()
+            w_tok, w_len, w_pr = w_tok.cpu().numpy(), w_len.cpu().numpy(), w_pr.cpu().numpy()
+            t0 = full.cu_draft[:-1].astype(np.int64) + np.arange(full.B)
+            same = np.array_equal(w_len, g_len) and all(
+                np.array_equal(w_tok[t0[i]:t0[i] + w_len[i]], g_tok[t0[i]:t0[i] + g_len[i]]) for i in range(full.B))
+            strong = {"ranks": world, "global_requests": full.B, "global_rows": full.R_t,
+                      "equal_to_one_verify_of_the_batch": bool(same),
+                      "max_prob_diff": float(np.max(np.abs(w_pr - g_pr)))}
+            del dfull
 
     peaks = measured_peaks()
     if peaks and "hbm_gbs" in peaks:
@@ -352,16 +392,19 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD if B == 256 else WORKLOAD.replace("B=256", f"B={B}"), "B": B, "K": 7, "V": batch.V, "temperature": batch.temperature,
+        "scaling": "strong" if args.strong else "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD if args.batch == 256 else WORKLOAD.replace("B=256", f"B={args.batch}"),
+                   "B": args.batch, "K": 7, "V": batch.V, "temperature": batch.temperature,
                    "logits": "bf16", "rows_per_step": R_t, "draft_rows_per_step": batch.R_d,
                    "algorithmic_bytes_per_step": alg_bytes,
                    "l2": "inputs 1.17 GB > 129 MB L2 per step: no flush needed",
-                   "parallelism": f"requests sharded, {world} rank(s), no collective"},
-        "committed_tokens_per_s": committed * world / (ms_per_step * 1e-3),
+                   "parallelism": (f"one batch split by requests over {world} rank(s); outputs gathered after "
+                                   "the timed region" if args.strong else
+                                   f"requests sharded, {world} rank(s), no collective")},
+        "committed_tokens_per_s": committed / (ms_per_step * 1e-3),
         "hbm_gbs": achieved,
         "acceptance": {"draft_acceptance_rate": accepted / int(K.sum()),
-                       "mean_acceptance_length": committed / B},
+                       "mean_acceptance_length": mean_len},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                      "traffic_source": TRAFFIC["profile"] if traffic else None,
@@ -374,6 +417,8 @@ def run_ours(args):
         "parity_spot_check": spot,
         "wall_s_timed_region": t_wall,
     }
+    if strong is not None:
+        line["strong_check"] = strong
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
@@ -697,6 +742,8 @@ def main():
                     help="requests of the batch the CPU baseline times (default: all)")
     ap.add_argument("--cpu-reps", type=int, default=3)
     ap.add_argument("--ref-budget-s", type=float, default=100.0)
+    ap.add_argument("--strong", action="store_true",
+                    help="split one global batch over the ranks (strong scaling) instead of one batch per rank")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="verify_b256", choices=["verify_b256", *EXTRA_WORKLOADS],

@@ -94,3 +94,15 @@ def merge_outputs(parts):
     ln = np.concatenate([p[1] for p in parts])
     pr = None if parts[0][2] is None else np.concatenate([p[2] for p in parts])
     return tok, ln, pr
+
+
+def gather_outputs(tok, ln, pr, group=None):
+    """Every rank's shard outputs (numpy out_tokens, out_len, out_probs or
+    None), gathered over a torch.distributed group and concatenated in rank
+    order: the global outputs, on every rank. The arrays are a few KB per
+    rank (tokens and lengths), so they travel as pickled objects."""
+    import torch.distributed as dist
+
+    parts = [None] * dist.get_world_size(group)
+    dist.all_gather_object(parts, (tok, ln, pr), group=group)
+    return merge_outputs(parts)

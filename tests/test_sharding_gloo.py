@@ -79,20 +79,18 @@ def _rank_main(rank, world, port, out_path):
         bounds = S.partition_requests(b.cu_draft, world, b.greedy_mask(), b.draft is not None)
         shard = S.shard_of(b.cu_draft, int(bounds[rank]), int(bounds[rank + 1]))
         res = parity.oracle_verify(S.local_batch(b, shard), nthreads=1)
-        mine = (res.out_tokens.tolist(), res.out_len.tolist(), res.out_probs.tolist())
-        parts = [None] * world
-        dist.all_gather_object(parts, mine)
+        merged = S.gather_outputs(res.out_tokens, res.out_len, res.out_probs)
+        sizes = [None] * world
+        dist.all_gather_object(sizes, int(shard.B))
         slowest = bench.max_over_ranks(1.5 + rank, "cpu")
         seeds = [None] * world
         dist.all_gather_object(seeds, bench.rank_seed(3, rank))
         if rank == 0:
-            merged = S.merge_outputs([(np.array(t), np.array(l), np.array(p)) for t, l, p in parts])
             whole = parity.oracle_verify(b, nthreads=1)
             ok = (np.array_equal(merged[0], whole.out_tokens) and np.array_equal(merged[1], whole.out_len)
                   and np.array_equal(merged[2], whole.out_probs))
             with open(out_path, "w") as f:
-                json.dump({"equal": bool(ok), "slowest": slowest, "seeds": seeds,
-                           "sizes": [len(p[1]) for p in parts]}, f)
+                json.dump({"equal": bool(ok), "slowest": slowest, "seeds": seeds, "sizes": sizes}, f)
         dist.barrier()
     finally:
         dist.destroy_process_group()
