@@ -802,15 +802,19 @@ __device__ bool stream_collect(FtSmem& s, const void* row, int V, bool vec, int 
   return true;
 }
 
+// Returns the row's threshold. kept_in_buf: s.cand[0, n_buf) holds every
+// logit the threshold keeps (and maybe more below it); M_row: the row's
+// maximum (when kept_in_buf).
 template <int DT>
 __device__ float row_threshold(FtSmem& s, const void* rowp, int V, bool vec, int top_k, float top_p,
-                               float c) {
+                               float c, bool& kept_in_buf, int& n_buf, float& M_row) {
   constexpr int KB = DT == 1 ? 16 : 32;  // key bits
   const bool use_k = top_k >= 1 && top_k < V;
   const bool use_p = top_p > 0.f && top_p < 1.f;
   const RowSrc<DT> row{rowp, V, vec};
   CandSrc<DT> cs{s.cand, 0};
   bool in_smem = false;  // the candidates hold every key still in play
+  kept_in_buf = false;
   uint32_t floor = 0u;   // keys >= floor are kept
   float M = -INFINITY;
   bool mass_known = false;  // s.row_mass holds the row's mass relative to M
@@ -840,6 +844,7 @@ __device__ float row_threshold(FtSmem& s, const void* rowp, int V, bool vec, int
       }
     }
     floor = prefix;
+    M_row = M;
   }
   if (use_p) {
     if (!use_k) {
@@ -853,6 +858,7 @@ __device__ float row_threshold(FtSmem& s, const void* rowp, int V, bool vec, int
       M = s.rowmax;
     }
     if (!(M > -INFINITY)) return -INFINITY;
+    M_row = M;
     // Masses are relative to 2^mc: the row maximum's scaled value, or the
     // one-pass collection's integer reference, which its left-out mass
     // shares.
@@ -882,8 +888,38 @@ __device__ float row_threshold(FtSmem& s, const void* rowp, int V, bool vec, int
     }
     if (prefix > floor) floor = prefix;
   }
+  // Every key >= floor is in the buffer once it holds the keys in play; a
+  // threshold of -inf keeps the whole row, which it then holds only if it
+  // holds all V logits.
+  n_buf = cs.n;
+  kept_in_buf = in_smem && M_row > -INFINITY && (floor != 0u || cs.n >= V);
   if (floor == 0u) return -INFINITY;
   return DT == 1 ? value16(floor) : value32(floor);
+}
+
+// Filtered softmax statistics of the row from the buffer (all threads; the
+// result is valid in thread 0): mc = fp32(M c), S = sum over the buffered
+// logits z >= tau of 2^(z c - mc), per thread in fp32, over the CTA in fp64.
+__device__ FStat buffer_stats(FtSmem& s, int n, float tau, float M, float c) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float mc = __fmul_rn(M, c);
+  float part = 0.f;
+  for (int j = threadIdx.x; j < n; j += kFtThreads) {
+    const float z = s.cand[j];
+    if (z >= tau) part += exp2f(fmaf(z, c, -mc));
+  }
+  double d = (double)part;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+  if (lane == 0) s.wsd[warp] = d;
+  __syncthreads();
+  FStat f;
+  f.mc = mc;
+  f.ok = 1;
+  f.S = 0.0;
+  for (int w = 0; w < kFtWarps; ++w) f.S += s.wsd[w];
+  __syncthreads();
+  return f;
 }
 
 // Rows [0, R_t) are target rows (request b at cu[b] + b + i); rows
@@ -911,13 +947,319 @@ __global__ void __launch_bounds__(kFtThreads, 3) threshold_kernel(FtParams P) {
         hi = mid - 1;
     }
     const bool greedy = P.mode && P.mode[lo] == SV_MODE_GREEDY;
+    // Rows the warp kernel finished (ok) keep its threshold and statistics.
+    if (P.after_warp && (greedy || (is_t ? P.fst_t : P.fst_d)[rr].ok)) continue;
     float tau = -INFINITY;
+    FStat fs{0.f, 0, 0.0};
     if (!greedy) {
       const char* row = static_cast<const char*>(is_t ? P.target : P.draft) + (size_t)rr * rowb;
-      tau = row_threshold<DT>(s, row, P.V, P.vec, P.top_k, P.top_p, P.c);
+      bool in_buf = false;
+      int n_buf = 0;
+      float M = -INFINITY;
+      tau = row_threshold<DT>(s, row, P.V, P.vec, P.top_k, P.top_p, P.c, in_buf, n_buf, M);
+      // The filtered row's softmax from the buffer: the verify kernel then
+      // need not read the row again.
+      if (in_buf && P.fst_t) fs = buffer_stats(s, n_buf, tau, M, P.c);
     }
-    if (threadIdx.x == 0) (is_t ? P.thr_t : P.thr_d)[rr] = tau;
+    if (threadIdx.x == 0) {
+      (is_t ? P.thr_t : P.thr_d)[rr] = tau;
+      if (P.fst_t) (is_t ? P.fst_t : P.fst_d)[rr] = fs;
+    }
     __syncthreads();
+  }
+}
+
+
+// ---------------------------------------------------------------------------
+// One warp per row (top-k up to kWarpMaxK, with or without top-p)
+// ---------------------------------------------------------------------------
+// Every row streams at once (one wave of warps), and each warp selects its
+// row's threshold alone, with no CTA barrier. The warp keeps a buffer of the
+// logits at or above a floor that never exceeds the k-th largest logit
+// seen: the k-th largest of the lanes' kWTop largest vector maxima (k of
+// those maxima, each a logit, lie at or above it), raised after iterations
+// 0, 1, 3, 7, ... and to the k-th largest buffered logit when the buffer
+// passes half full. After the pass the buffer holds every logit the
+// threshold keeps:
+//   top-k: the k-th largest buffered key (bit by bit, counts over the warp);
+//   top-p: walking the distinct kept values from the largest down, summing
+//     their masses 2^(z c - mc) (mc = fp32(M c), M the row maximum) in the
+//     same 2^-44 fixed point as the CTA kernel's bins (exact, so its sums
+//     and this walk agree), up to the first value at which the mass reaches
+//     p times the kept mass.
+// Rows the warp cannot finish (a buffer that stays more than half full: long
+// tie groups, or no finite logit) are left with ok = 0 for the CTA kernel,
+// which then skips the rows marked ok.
+constexpr int kWarpMaxK = 128;
+constexpr int kWTop = 4;          // vector maxima each lane tracks: k <= 32 * kWTop
+constexpr int kWCap = 512;        // logits a warp's buffer holds
+constexpr int kWLoads = 8;        // 16-byte vectors a lane has in flight
+static_assert(kWarpMaxK <= 32 * kWTop, "k of the tracked maxima must exist");
+
+// 16-byte streaming load that does not allocate in L1 (read once).
+__device__ __forceinline__ uint4 wt_ld16(const uint4* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float wt_max(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Largest key `x` such that at least k of the warp's values have key >= x
+// (the k-th largest key), over n_per_lane values per lane (keys given).
+template <int DT, int N>
+__device__ __forceinline__ uint32_t warp_kth_key(const uint32_t (&keys)[N], int k) {
+  constexpr int KB = DT == 1 ? 16 : 32;
+  uint32_t prefix = 0u;
+#pragma unroll 1
+  for (int bit = KB - 1; bit >= 0; --bit) {
+    const uint32_t cand = prefix | (1u << bit);
+    unsigned c = 0;
+#pragma unroll
+    for (int j = 0; j < N; ++j) c += keys[j] >= cand ? 1u : 0u;
+    if ((int)__reduce_add_sync(0xffffffffu, c) >= k) prefix = cand;
+  }
+  return prefix;
+}
+
+// The k-th largest key among the buffer's n logits (lane-strided).
+template <int DT>
+__device__ uint32_t buffer_kth_key(const float* buf, unsigned n, int k) {
+  constexpr int KB = DT == 1 ? 16 : 32;
+  const int lane = threadIdx.x & 31;
+  uint32_t prefix = 0u;
+#pragma unroll 1
+  for (int bit = KB - 1; bit >= 0; --bit) {
+    const uint32_t cand = prefix | (1u << bit);
+    unsigned c = 0;
+    for (unsigned j = lane; j < n; j += 32) c += key_of<DT>(buf[j]) >= cand ? 1u : 0u;
+    if ((int)__reduce_add_sync(0xffffffffu, c) >= k) prefix = cand;
+  }
+  return prefix;
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int DT>
+__device__ __forceinline__ float value_of_key(uint32_t k) {
+  return DT == 1 ? value16(k) : value32(k);
+}
+
+struct WarpRowSmem {
+  float buf[kFtWarps][kWCap];
+  unsigned n[kFtWarps];
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kFtThreads, 4) threshold_warp_kernel(FtParams P) {
+  constexpr int EV = DT == 1 ? 8 : 4;  // logits per 16-byte vector
+  __shared__ WarpRowSmem sm;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* buf = sm.buf[warp];
+  unsigned* nb = &sm.n[warp];
+  int R_d = P.cu[P.B], R_t = R_d + P.B;
+  if (R_t > P.rows_t || R_d < 0) R_t = R_d = 0;
+  const int rows = R_t + (P.draft ? R_d : 0);
+  const size_t rowb = (size_t)P.V * (DT == 1 ? 2 : 4);
+  const int k = P.top_k;
+  const bool use_p = P.top_p > 0.f && P.top_p < 1.f;
+  const int nvec = P.V / EV;
+  for (int r = blockIdx.x * kFtWarps + warp; r < rows; r += gridDim.x * kFtWarps) {
+    const bool is_t = r < R_t;
+    const int rr = is_t ? r : r - R_t;
+    int greedy = 0;
+    if (lane == 0 && P.mode) {
+      int lo = 0, hi = P.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((is_t ? P.cu[mid] + mid : P.cu[mid]) <= rr) lo = mid; else hi = mid - 1;
+      }
+      greedy = P.mode[lo] == SV_MODE_GREEDY;
+    }
+    greedy = __shfl_sync(0xffffffffu, greedy, 0);
+    FStat out{0.f, 0, 0.0};
+    float tau = -INFINITY;
+    if (!greedy) {
+      const uint4* row = reinterpret_cast<const uint4*>(static_cast<const char*>(is_t ? P.target : P.draft) +
+                                                        (size_t)rr * rowb);
+      if (lane == 0) *nb = 0u;
+      __syncwarp();
+      float top[kWTop];
+#pragma unroll
+      for (int j = 0; j < kWTop; ++j) top[j] = -INFINITY;
+      float rmax = -INFINITY, fl = -INFINITY;
+      bool ovf = false;
+      int it = 0;
+      for (int base = 0; base < nvec; base += 32 * kWLoads, ++it) {
+        uint4 w[kWLoads];
+#pragma unroll
+        for (int u = 0; u < kWLoads; ++u) {
+          const int j = base + u * 32 + lane;
+          w[u] = j < nvec ? wt_ld16(row + j) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+          if (DT == 0 && j >= nvec) w[u] = make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+        }
+        float vm[kWLoads];
+#pragma unroll
+        for (int u = 0; u < kWLoads; ++u) {
+          if (DT == 1) {
+            uint32_t m2 = bf2_max(bf2_max(w[u].x, w[u].y), bf2_max(w[u].z, w[u].w));
+            vm[u] = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xffff0000u));
+          } else {
+            vm[u] = fmaxf(fmaxf(__uint_as_float(w[u].x), __uint_as_float(w[u].y)),
+                          fmaxf(__uint_as_float(w[u].z), __uint_as_float(w[u].w)));
+          }
+          rmax = fmaxf(rmax, vm[u]);
+          // Keep this lane's kWTop largest vector maxima (sorted, largest first).
+          if (vm[u] > top[kWTop - 1]) {
+            float x = vm[u];
+#pragma unroll
+            for (int j = 0; j < kWTop; ++j) {
+              const float hi = fmaxf(top[j], x);
+              x = fminf(top[j], x);
+              top[j] = hi;
+            }
+          }
+        }
+        // Raise the floor at iterations 0, 1, 3, 7, ...: k of the tracked
+        // maxima lie at or above their k-th largest.
+        if ((it & (it + 1)) == 0) {
+          uint32_t keys[kWTop];
+#pragma unroll
+          for (int j = 0; j < kWTop; ++j) keys[j] = key_of<DT>(top[j]);
+          fl = fmaxf(fl, value_of_key<DT>(warp_kth_key<DT, kWTop>(keys, k)));
+        }
+        // Append the logits at or above the floor.
+#pragma unroll
+        for (int u = 0; u < kWLoads; ++u) {
+          if (vm[u] >= fl) {
+            const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+#pragma unroll
+              for (int h = 0; h < (DT == 1 ? 2 : 1); ++h) {
+                const float z = DT == 1 ? __uint_as_float(h ? (ws[q] & 0xffff0000u) : (ws[q] << 16))
+                                        : __uint_as_float(ws[q]);
+                if (z >= fl) {
+                  const unsigned pos = atomicAdd(nb, 1u);
+                  if (pos < (unsigned)kWCap) buf[pos] = z; else ovf = true;
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+        // Every branch below that leads to a warp collective is taken by the
+        // whole warp: the overflow flag is made uniform first.
+        ovf = __any_sync(0xffffffffu, ovf);
+        if (ovf) break;
+        unsigned n = *nb;
+        if (n > (unsigned)(kWCap / 2)) {
+          // Raise the floor to the k-th largest buffered logit and compact.
+          fl = fmaxf(fl, value_of_key<DT>(buffer_kth_key<DT>(buf, n, k)));
+          __syncwarp();
+          float keep[kWCap / 32];
+          int nk = 0;
+#pragma unroll
+          for (int j = 0; j < kWCap / 32; ++j) {
+            const unsigned idx = (unsigned)(j * 32 + lane);
+            const float z = idx < n ? buf[idx] : -INFINITY;
+            keep[j] = z;
+            nk += (idx < n && z >= fl) ? 1 : 0;
+          }
+          // Exclusive prefix of the kept counts over the lanes.
+          int incl = nk;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+          }
+          const int total = __shfl_sync(0xffffffffu, incl, 31);
+          int pos = incl - nk;
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < kWCap / 32; ++j) {
+            const unsigned idx = (unsigned)(j * 32 + lane);
+            if (idx < n && keep[j] >= fl) buf[pos++] = keep[j];
+          }
+          if (lane == 0) *nb = (unsigned)total;
+          __syncwarp();
+          if (total > kWCap / 2) {  // a tie group at the floor that does not fit
+            ovf = true;
+            break;
+          }
+        }
+      }
+      rmax = wt_max(rmax);
+      const unsigned n = min(*nb, (unsigned)kWCap);
+      if (!ovf && rmax > -INFINITY && (int)n >= k) {
+        // Top-k: the k-th largest buffered key; every logit at or above it
+        // is in the buffer.
+        uint32_t tk = buffer_kth_key<DT>(buf, n, k);
+        float tv = value_of_key<DT>(tk);
+        const float mc = __fmul_rn(rmax, P.c);
+        if (use_p) {
+          // Top-p on the top-k set, distinct values from the largest down.
+          unsigned long long tot = 0ull;
+          for (unsigned j = lane; j < n; j += 32) {
+            const float z = buf[j];
+            if (z >= tv) tot += __float2ull_rn(exp2f(fmaf(z, P.c, -mc)) * 0x1p44f);
+          }
+          tot = warp_sum_u64(tot);
+          const double need = (double)P.top_p * ((double)tot * 0x1p-44);
+          unsigned long long cum = 0ull;
+          float cur = INFINITY, pick = tv;
+#pragma unroll 1
+          for (;;) {
+            float v = -INFINITY;
+            for (unsigned j = lane; j < n; j += 32) {
+              const float z = buf[j];
+              if (z >= tv && z < cur) v = fmaxf(v, z);
+            }
+            v = wt_max(v);
+            if (v == -INFINITY) break;  // no value left: everything in play stays
+            unsigned long long g = 0ull;
+            for (unsigned j = lane; j < n; j += 32) {
+              const float z = buf[j];
+              if (z == v) g += __float2ull_rn(exp2f(fmaf(z, P.c, -mc)) * 0x1p44f);
+            }
+            cum += warp_sum_u64(g);
+            pick = v;
+            if ((double)cum * 0x1p-44 >= need) break;
+            cur = v;
+          }
+          if (pick > tv) tv = pick;
+        }
+        tau = tv;
+        // The filtered row's softmax sum from the buffer.
+        float part = 0.f;
+        for (unsigned j = lane; j < n; j += 32) {
+          const float z = buf[j];
+          if (z >= tau) part += exp2f(fmaf(z, P.c, -mc));
+        }
+        double d = (double)part;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        out.mc = mc;
+        out.ok = 1;
+        out.S = d;
+      }
+    }
+    if (lane == 0) {
+      // Rows left with ok = 0 get their threshold from the CTA kernel.
+      if (out.ok || greedy) (is_t ? P.thr_t : P.thr_d)[rr] = tau;
+      (is_t ? P.fst_t : P.fst_d)[rr] = out;
+    }
+    __syncwarp();
   }
 }
 
@@ -939,12 +1281,28 @@ static cudaError_t launch_thresholds_t(const FtParams& P, int sms, cudaStream_t 
   return cudaGetLastError();
 }
 
-cudaError_t launch_thresholds(const FtParams& P, int dtype, cudaStream_t st) {
+cudaError_t launch_thresholds(const FtParams& P0, int dtype, cudaStream_t st) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  FtParams P = P0;
+  P.after_warp = false;
+  // Top-k up to kWarpMaxK on vector rows: one warp per row first; the CTA
+  // kernel then takes only the rows it left.
+  if (P.fst_t && P.vec && P.top_k >= 1 && P.top_k <= kWarpMaxK) {
+    const int rows = 2 * P.rows_t;
+    int grid = (rows + kFtWarps - 1) / kFtWarps;
+    if (grid < 1) grid = 1;
+    if (dtype == SV_BF16)
+      threshold_warp_kernel<1><<<grid, kFtThreads, 0, st>>>(P);
+    else
+      threshold_warp_kernel<0><<<grid, kFtThreads, 0, st>>>(P);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    P.after_warp = true;
+  }
   return dtype == SV_BF16 ? launch_thresholds_t<1>(P, sms, st) : launch_thresholds_t<0>(P, sms, st);
 }
 

@@ -190,6 +190,8 @@ struct Params {
   double* btile;            // [B, tsum_stride] tile sums of a bonus row's r = S_p p
   const float* thr;         // [R_t] filter thresholds of the target rows, or NULL
   const float* thr_d;       // [R_d] filter thresholds of the draft rows, or NULL
+  const FStat* fst;         // [R_t] filtered softmax statistics of the target rows, or NULL
+  const FStat* fst_d;       // [R_d] of the draft rows, or NULL
   int n_slots, tsum_stride;
   unsigned int* part_done;  // [kMaxTailRows] parts finished per split row
   PartRec* parts;           // [kMaxPartRecs]
@@ -206,6 +208,7 @@ struct Smem {
   unsigned n_items, r_full, row_parts;  // work-item layout of this launch
   int b, t, t0, d0, K, i, greedy, xhat, last, stop, merge, pick, pick2, tok, R_d;
   int zx_ok;        // z_p(x̂) (and z_q(x̂)) were taken from the ring during the row pass
+  int pre;          // filtered row: its statistics came from the threshold kernel
   int btile_ok;     // this bonus row's tile sums were stored during its pass
   float tau_t, tau_d;  // filter thresholds of the row pair (-inf: unfiltered)
   float zx_p, zx_q, u_acc;
@@ -1610,7 +1613,37 @@ __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int 
   }
   PartRec st;
   const bool btiles = VEC && i == K && !greedy;
-  if (!slice_stats<DT, VEC>(P, s, ring, trow, drow, greedy, c0, c1, st, btiles, b)) return false;
+  bool pre = false;
+  if constexpr ((DT & kFilt) != 0) {
+    // A whole filtered row whose threshold kernel left its statistics (and
+    // its draft row's) is not read again: the accept test needs only z(x̂)
+    // of each row, two scalar loads.
+    if (part < 0 && P.fst) {
+      if (tid == 0) {
+        const FStat ft = P.fst[t];
+        const FStat fd = has_d ? P.fst_d[d0 + i] : FStat{0.f, 1, 0.0};
+        int ok = !greedy && ft.ok && fd.ok;
+        if (ok) {
+          st.mc_p = ft.mc;
+          st.S_p = ft.S;
+          st.mc_q = has_d ? fd.mc : 0.f;
+          st.S_q = has_d ? fd.S : 0.0;
+          st.amax_v = -INFINITY;
+          st.amax_i = 0x7fffffff;
+          const int xh = s.xhat;
+          if (i < K && xh >= 0) {
+            s.zx_p = mask_below<DT>(Elem<DT & 1>::scalar(trow, xh), s.tau_t);
+            if (has_d) s.zx_q = mask_below<DT>(Elem<DT & 1>::scalar(drow, xh), s.tau_d);
+            s.zx_ok = 1;
+          }
+        }
+        s.pre = ok;
+      }
+      __syncthreads();
+      pre = s.pre != 0;
+    }
+  }
+  if (!pre && !slice_stats<DT, VEC>(P, s, ring, trow, drow, greedy, c0, c1, st, btiles, b)) return false;
   if (part >= 0) {
     if (tid == 0) {
       P.parts[(size_t)split * np + part] = st;
@@ -1881,7 +1914,8 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
                             int32_t* out_tokens, int32_t* out_len, float* out_probs,
                             void* workspace, size_t workspace_bytes, void* stream,
                             int greedy_all, const float* thr = nullptr,
-                            const float* thr_d = nullptr) {
+                            const float* thr_d = nullptr, const FStat* fst = nullptr,
+                            const FStat* fst_d = nullptr) {
   const sv_status chk = check_verify_args(target, draft, dtype, V, B, draft_tokens, cu_draft, uniforms,
                                           temperature, out_tokens, out_len, out_probs, greedy_all);
   if (chk != SV_OK || B == 0) return chk;
@@ -1919,6 +1953,8 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
   P.greedy_all = greedy_all;
   P.thr = thr;
   P.thr_d = thr_d;
+  P.fst = fst;
+  P.fst_d = fst_d;
 
   // Bulk copies need 16-byte aligned row starts and 16-byte multiples.
   const bool vec = ((uintptr_t)target % 16 == 0) && (!P.draft || (uintptr_t)P.draft % 16 == 0) &&
@@ -1997,10 +2033,13 @@ sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logit
   return SV_OK;
 }
 
-// Filtered form: the per-row thresholds come first in the workspace, then
-// the verify kernel's own workspace.
-static size_t filter_bytes(int64_t R_t, int64_t B) {
+// Filtered form: the per-row thresholds and filtered statistics come first
+// in the workspace, then the verify kernel's own workspace.
+static size_t filter_thr_bytes(int64_t R_t, int64_t B) {
   return sv::align16((size_t)R_t * 4) + sv::align16((size_t)(R_t - B) * 4 + 4);
+}
+static size_t filter_bytes(int64_t R_t, int64_t B) {
+  return filter_thr_bytes(R_t, B) + (size_t)R_t * sizeof(sv::FStat) + (size_t)(R_t - B + 1) * sizeof(sv::FStat);
 }
 
 size_t spec_verify_filtered_workspace_size(int32_t B, int32_t R_t, int32_t V) {
@@ -2047,12 +2086,14 @@ sv_status spec_verify_filtered(const void* target_logits, const void* draft_logi
            (((size_t)V * es) % 16 == 0);
   fp.thr_t = reinterpret_cast<float*>(ws);
   fp.thr_d = reinterpret_cast<float*>(ws + sv::align16((size_t)R_t * 4));
+  fp.fst_t = reinterpret_cast<sv::FStat*>(ws + filter_thr_bytes(R_t, B));
+  fp.fst_d = fp.fst_t + R_t;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   if (sv::launch_thresholds(fp, dtype, st) != cudaSuccess) return SV_ERR_CUDA;
   return sv::run_verify(target_logits, draft_logits, dtype, V, B, draft_tokens, cu_draft, mode,
                         uniforms, temperature, out_tokens, out_len, out_probs, ws + fb,
                         workspace_bytes - fb, cuda_stream, 0, fp.thr_t,
-                        draft_logits ? fp.thr_d : nullptr);
+                        draft_logits ? fp.thr_d : nullptr, fp.fst_t, draft_logits ? fp.fst_d : nullptr);
 }
 
 size_t spec_verify_workspace_size(int32_t B, int32_t R_t, int32_t V) {

@@ -174,3 +174,36 @@ def test_filtered_rerun_is_bit_identical(cuda_lib, top_k, top_p):
             runs.append((tok.clone(), ln.clone(), pr.clone()))
         for r in runs[1:]:
             assert all(torch.equal(x, y) for x, y in zip(runs[0], r))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("top_k,top_p", [(50, 1.0), (128, 0.9), (129, 0.9), (8, 0.6)])
+def test_warp_rows_and_fallback_rows_in_one_batch(cuda_lib, dtype, top_k, top_p):
+    """Top-k up to 128 goes to the one-warp-per-row kernel first; rows it
+    cannot finish (here: rising rows whose values all pass the floor, and
+    rows of one value) go to the CTA kernel, which skips the rest. Peaked,
+    rising and constant rows alternate in one batch; k = 129 takes the CTA
+    kernel alone."""
+    rng = np.random.default_rng(570 + top_k)
+    V = 40000
+    b = W.gaussian_sampling(seed=571 + top_k, B=8, K=3, V=V, sigma=2.0, draft_sigma=0.5, T=1.0)
+    R = b.R_t
+    x = np.arange(V, dtype=np.float64)
+    zt = np.empty((R, V))
+    for r in range(R):
+        kind = r % 3
+        if kind == 0:   # peaked: a random permutation of rank scores
+            zt[r, rng.permutation(V)] = -4.4 * np.log(np.arange(1, V + 1)) + rng.normal(0, 1, V)
+        elif kind == 1:  # rising: every chunk beats the floor
+            zt[r] = -6.0 + 12.0 * x / V + rng.normal(0, 0.01, V)
+        else:            # one value: a tie group of the whole row
+            zt[r] = 0.5
+    zt = zt.astype(np.float32)
+    rows_d = np.concatenate([np.arange(b.cu_draft[i] + i, b.cu_draft[i] + i + 3) for i in range(b.B)])
+    zd = (zt[rows_d] + rng.normal(0, 0.3, (rows_d.size, V))).astype(np.float32)
+    if dtype == "bf16":
+        b.target, b.draft = W.to_bf16_bits(zt), W.to_bf16_bits(zd)
+    else:
+        b.target, b.draft = zt, zd
+    rep = _run(b, top_k, top_p)
+    assert rep.mismatched_requests <= 1
