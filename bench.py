@@ -446,6 +446,9 @@ EXTRA_WORKLOADS = {
                     "counter block",
     "topkp_b256": "top-k 50 / top-p 0.9 filtered sampling verify on the benchmark batch (B=256 K=7 "
                   "V=151936 bf16 T=0.7, peaked rank-score rows)",
+    "vshard_b256x2": "vocabulary-sharded verify of the benchmark batch (B=256 K=7 V=151936 bf16 T=0.7, peaked "
+                     "rows) split over 2 vocabulary shards held by one process on one GPU (shard kernels and "
+                     "the local exchanges; no interconnect)",
     "candidates_b64x4": "64 requests x 4 draft candidates of 5 tokens (V=32000 bf16, T=1.0), verified as "
                         "256 requests, then one kept per request by its selection uniform (lossless rule)",
 }
@@ -544,7 +547,7 @@ def _extra_setup(name, seed):
         batches = [W.config4_verify(seed=seed, proposals=o[0], counts=o[1])]
     elif name == "ragged_b512":
         batches = [W.config5(seed=seed)]
-    elif name == "topkp_b256":
+    elif name in ("topkp_b256", "vshard_b256x2"):
         batches = [W.config3(seed=seed)]
     elif name == "candidates_b64x4":
         batches = [W.gaussian_sampling(seed=seed, B=256, K=5, V=32000, sigma=2.0, draft_sigma=0.5, T=1.0,
@@ -561,6 +564,13 @@ def _extra_setup(name, seed):
     k = [0]
     greedy_only = name == "greedy_b64"
     filtered = name == "topkp_b256"
+    sharded = name == "vshard_b256x2"
+    if sharded:
+        from speculative_decoding_verification_27_gb300 import vshard
+        bounds = vshard.split_vocab(b0.V, 2)
+        d0_ = dbs[0]
+        shards = [vshard.Shard(d0_.target[:, a:c].contiguous(), d0_.draft[:, a:c].contiguous(), a)
+                  for a, c in zip(bounds[:-1], bounds[1:])]
     cands = name == "candidates_b64x4"
     if cands:
         cu_cand = torch.arange(0, 257, 4, dtype=torch.int32, device="cuda")
@@ -578,6 +588,9 @@ def _extra_setup(name, seed):
             api.spec_verify_filtered(db.target, db.draft, db.draft_tokens, db.cu_draft, db.uniforms,
                                      db.temperature, FILTER_K, FILTER_P, db.mode, out_tokens=ot, out_len=ol,
                                      out_probs=op, workspace=ws)
+        elif sharded:
+            vshard.spec_verify_vsharded(shards, b0.V, db.draft_tokens, db.cu_draft, db.uniforms, db.temperature,
+                                        db.mode, out_tokens=ot, out_len=ol, out_probs=op)
         elif greedy_only:
             api.spec_verify_greedy(db.target, db.draft_tokens, db.cu_draft, out_tokens=ot, out_len=ol,
                                    workspace=ws)
@@ -591,6 +604,12 @@ def _extra_setup(name, seed):
     d0 = dbs[0]
     host = {f: (getattr(d0, f), getattr(d0, f).cpu().pin_memory())
             for f in ("target", "draft", "draft_tokens", "cu_draft", "uniforms") if getattr(d0, f) is not None}
+    if sharded:  # the step reads the shards' slices, not the whole matrices
+        for f in ("target", "draft"):
+            del host[f]
+        for j, sh in enumerate(shards):
+            host[f"target{j}"] = (sh.target, sh.target.cpu().pin_memory())
+            host[f"draft{j}"] = (sh.draft, sh.draft.cpu().pin_memory())
     sample = b0 if b0.B <= 64 else oracle_sample(b0, 64)
 
     def oracle_run(diagnostics):
@@ -629,7 +648,9 @@ def _extra_setup(name, seed):
     if filtered:
         desc.update({"top_k": FILTER_K, "top_p": FILTER_P})
     outs = [ot, ol] if not cands else [ot, ol, best, best_len]
-    return desc, host, outs, step, units, "rows/s", nbytes, name not in ("ragged_b512", "topkp_b256"), \
+    if sharded:
+        desc.update({"shards": 2, "shard_bounds": bounds})
+    return desc, host, outs, step, units, "rows/s", nbytes, name not in ("ragged_b512", "topkp_b256", "vshard_b256x2"), \
         oracle_fn, check
 
 
@@ -720,6 +741,7 @@ def run_extra(args):
                                    else spot["rows"]) / dt,
                          "unit": unit, "cores": threads, "kind": "oracle",
                          "sample": {"ragged_b512": "64 of 512 requests", "topkp_b256": "64 of 256 requests",
+                                    "vshard_b256x2": "64 of 256 requests (whole vocabulary)",
                                     "candidates_b64x4": "64 of 256 candidates (verify only)"}.get(
                                         args.workload, "the whole step")},
         "parity_spot_check": spot,
