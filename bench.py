@@ -44,12 +44,12 @@ WORKLOAD = ("sampling verify B=256 K=7 V=151936 bf16 T=0.7, peaked rank-score ro
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per verify launch on this workload from one ncu
 # capture, valid only for the kernel sources whose hash is recorded with it.
-TRAFFIC = {"sources_sha256": "1007868c993b0dfb0c790d500e8b8131450ccd99353df1dd31aacf3648e948be",
-           "bytes_per_launch": 1236024000 + 4343552,
+TRAFFIC = {"sources_sha256": "cef7f254000bddb4841b0f10ae9d59a5574c4671265a3f24be03cd1f20296402",
+           "bytes_per_launch": 1235726592 + 4355840,
            "profile": "profiles/verify_kernel_sampling_B256_K7_V151936_bf16.md"}
 
 
-VERIFY_SOURCES = ("spec_verify.cu", "sv_device.cuh")
+VERIFY_SOURCES = ("spec_verify.cu", "sv_device.cuh", "sv_filter.cuh")
 
 
 def kernel_sources_hash(names=VERIFY_SOURCES) -> str:

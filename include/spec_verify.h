@@ -181,16 +181,25 @@ sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype, int32_t 
  *   top_k, top_p  the filters (top_k >= 0, top_p > 0).
  *   workspace  >= spec_verify_filtered_workspace_size(B, R_t, V) bytes,
  *              16-byte aligned, zero-filled before first use.
- * Per row, a threshold kernel finds the row's threshold by a radix select on
- * order-preserving keys: counts for top-k, masses 2^(z c - M c) for top-p,
- * summed exactly in 64-bit fixed point from their fp32 values. For top-k up
- * to 256, and for top-p alone, the row is read once: the logits that can be
- * kept are collected in shared memory and the select runs on them. Rows
- * whose candidates do not fit (long tie groups at the threshold, or flat
- * rows under top-p, whose nucleus is a large part of the row) and larger k
- * take several passes over the row. The verify kernel then runs with every
- * logit below its row's threshold counted as -inf. A top-p decision within
- * about 1e-6 of its boundary can differ from a float64 evaluation.
+ * Per row, the threshold step finds the row's threshold:
+ *   - top-k up to 128 on 16-byte-aligned rows whose width is a multiple of
+ *     16 bytes: one warp per row reads the row once, collects the logits
+ *     that can be kept in shared memory and takes the k-th largest of them
+ *     (top-p then cuts that set). From the same buffer it leaves the
+ *     filtered row's softmax statistics and, for target rows, the list of
+ *     kept (token, logit) pairs, so the verify kernel does not read those
+ *     rows again: a draw from such a row reads the list and, for a
+ *     residual, the draft row at the listed tokens;
+ *   - other rows (and rows whose kept logits do not fit that buffer): a
+ *     CTA per row by a radix select on order-preserving keys, counts for
+ *     top-k and masses 2^(z c - M c) for top-p, summed exactly in 64-bit
+ *     fixed point from their fp32 values. For top-k up to 256, and for
+ *     top-p alone, the row is read once; rows whose candidates do not fit
+ *     (long tie groups at the threshold, or flat rows under top-p) and
+ *     larger k take several passes over the row.
+ * The verify kernel then counts every logit below its row's threshold as
+ * -inf. A top-p decision within about 1e-6 of its boundary can differ from
+ * a float64 evaluation.
  */
 size_t spec_verify_filtered_workspace_size(int32_t B, int32_t R_t, int32_t V);
 sv_status spec_verify_filtered(const void* target_logits, const void* draft_logits,

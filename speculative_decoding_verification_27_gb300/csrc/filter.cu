@@ -913,7 +913,7 @@ __device__ FStat buffer_stats(FtSmem& s, int n, float tau, float M, float c) {
   for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
   if (lane == 0) s.wsd[warp] = d;
   __syncthreads();
-  FStat f;
+  FStat f{};
   f.mc = mc;
   f.ok = 1;
   f.S = 0.0;
@@ -950,7 +950,7 @@ __global__ void __launch_bounds__(kFtThreads, 3) threshold_kernel(FtParams P) {
     // Rows the warp kernel finished (ok) keep its threshold and statistics.
     if (P.after_warp && (greedy || (is_t ? P.fst_t : P.fst_d)[rr].ok)) continue;
     float tau = -INFINITY;
-    FStat fs{0.f, 0, 0.0};
+    FStat fs{};
     if (!greedy) {
       const char* row = static_cast<const char*>(is_t ? P.target : P.draft) + (size_t)rr * rowb;
       bool in_buf = false;
@@ -1056,7 +1056,8 @@ __device__ __forceinline__ float value_of_key(uint32_t k) {
 }
 
 struct WarpRowSmem {
-  float buf[kFtWarps][kWCap];
+  float buf[kFtWarps][kWCap];  // buffered logits
+  int ix[kFtWarps][kWCap];     // their tokens
   unsigned n[kFtWarps];
 };
 
@@ -1066,6 +1067,7 @@ __global__ void __launch_bounds__(kFtThreads, 4) threshold_warp_kernel(FtParams 
   __shared__ WarpRowSmem sm;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float* buf = sm.buf[warp];
+  int* ix = sm.ix[warp];
   unsigned* nb = &sm.n[warp];
   int R_d = P.cu[P.B], R_t = R_d + P.B;
   if (R_t > P.rows_t || R_d < 0) R_t = R_d = 0;
@@ -1087,7 +1089,7 @@ __global__ void __launch_bounds__(kFtThreads, 4) threshold_warp_kernel(FtParams 
       greedy = P.mode[lo] == SV_MODE_GREEDY;
     }
     greedy = __shfl_sync(0xffffffffu, greedy, 0);
-    FStat out{0.f, 0, 0.0};
+    FStat out{};
     float tau = -INFINITY;
     if (!greedy) {
       const uint4* row = reinterpret_cast<const uint4*>(static_cast<const char*>(is_t ? P.target : P.draft) +
@@ -1138,20 +1140,27 @@ __global__ void __launch_bounds__(kFtThreads, 4) threshold_warp_kernel(FtParams 
           for (int j = 0; j < kWTop; ++j) keys[j] = key_of<DT>(top[j]);
           fl = fmaxf(fl, value_of_key<DT>(warp_kth_key<DT, kWTop>(keys, k)));
         }
-        // Append the logits at or above the floor.
+        // Append the logits at or above the floor, with their tokens.
 #pragma unroll
         for (int u = 0; u < kWLoads; ++u) {
           if (vm[u] >= fl) {
             const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+            const int x0 = (base + u * 32 + lane) * EV;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
 #pragma unroll
               for (int h = 0; h < (DT == 1 ? 2 : 1); ++h) {
+                // bf16: the low half of a word is the lower token.
                 const float z = DT == 1 ? __uint_as_float(h ? (ws[q] & 0xffff0000u) : (ws[q] << 16))
                                         : __uint_as_float(ws[q]);
                 if (z >= fl) {
                   const unsigned pos = atomicAdd(nb, 1u);
-                  if (pos < (unsigned)kWCap) buf[pos] = z; else ovf = true;
+                  if (pos < (unsigned)kWCap) {
+                    buf[pos] = z;
+                    ix[pos] = x0 + (DT == 1 ? 2 * q + h : q);
+                  } else {
+                    ovf = true;
+                  }
                 }
               }
             }
@@ -1164,32 +1173,26 @@ __global__ void __launch_bounds__(kFtThreads, 4) threshold_warp_kernel(FtParams 
         if (ovf) break;
         unsigned n = *nb;
         if (n > (unsigned)(kWCap / 2)) {
-          // Raise the floor to the k-th largest buffered logit and compact.
+          // Raise the floor to the k-th largest buffered logit and compact
+          // in place, 32 entries at a time: an entry only moves down, past
+          // entries already read.
           fl = fmaxf(fl, value_of_key<DT>(buffer_kth_key<DT>(buf, n, k)));
           __syncwarp();
-          float keep[kWCap / 32];
-          int nk = 0;
-#pragma unroll
-          for (int j = 0; j < kWCap / 32; ++j) {
-            const unsigned idx = (unsigned)(j * 32 + lane);
+          int total = 0;
+          for (unsigned j0 = 0; j0 < n; j0 += 32) {
+            const unsigned idx = j0 + lane;
             const float z = idx < n ? buf[idx] : -INFINITY;
-            keep[j] = z;
-            nk += (idx < n && z >= fl) ? 1 : 0;
-          }
-          // Exclusive prefix of the kept counts over the lanes.
-          int incl = nk;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-          }
-          const int total = __shfl_sync(0xffffffffu, incl, 31);
-          int pos = incl - nk;
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < kWCap / 32; ++j) {
-            const unsigned idx = (unsigned)(j * 32 + lane);
-            if (idx < n && keep[j] >= fl) buf[pos++] = keep[j];
+            const int x = idx < n ? ix[idx] : 0;
+            const bool kp = idx < n && z >= fl;
+            const unsigned bal = __ballot_sync(0xffffffffu, kp);
+            __syncwarp();
+            if (kp) {
+              const int pos = total + __popc(bal & ((1u << lane) - 1u));
+              buf[pos] = z;
+              ix[pos] = x;
+            }
+            total += __popc(bal);
+            __syncwarp();
           }
           if (lane == 0) *nb = (unsigned)total;
           __syncwarp();
@@ -1252,6 +1255,21 @@ __global__ void __launch_bounds__(kFtThreads, 4) threshold_warp_kernel(FtParams 
         out.mc = mc;
         out.ok = 1;
         out.S = d;
+        if (is_t && P.list_t) {
+          // The kept (token, logit) pairs of a target row, for its draw.
+          int2* lst = P.list_t + (size_t)rr * kKeptListCap;
+          int nk = 0;
+          for (unsigned j0 = 0; j0 < n; j0 += 32) {
+            const unsigned idx = j0 + lane;
+            const float z = idx < n ? buf[idx] : -INFINITY;
+            const bool kp = idx < n && z >= tau;
+            const unsigned bal = __ballot_sync(0xffffffffu, kp);
+            const int pos = nk + __popc(bal & ((1u << lane) - 1u));
+            if (kp && pos < kKeptListCap) lst[pos] = make_int2(ix[idx], __float_as_int(z));
+            nk += __popc(bal);
+          }
+          out.nl = nk <= kKeptListCap ? nk : 0;
+        }
       }
     }
     if (lane == 0) {

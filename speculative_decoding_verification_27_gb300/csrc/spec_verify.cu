@@ -34,6 +34,7 @@
 // Rows whose base is not 16-byte aligned (or whose byte length is not a
 // multiple of 16) take the same steps with scalar global loads.
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <cuda_bf16.h>
@@ -192,6 +193,7 @@ struct Params {
   const float* thr_d;       // [R_d] filter thresholds of the draft rows, or NULL
   const FStat* fst;         // [R_t] filtered softmax statistics of the target rows, or NULL
   const FStat* fst_d;       // [R_d] of the draft rows, or NULL
+  const int2* flist;        // [R_t, kKeptListCap] kept (token, logit bits) per target row, or NULL
   int n_slots, tsum_stride;
   unsigned int* part_done;  // [kMaxTailRows] parts finished per split row
   PartRec* parts;           // [kMaxPartRecs]
@@ -961,6 +963,69 @@ __device__ int draw_whole(const Params& P, Smem& s, unsigned char* ring, const D
   return locate_token<DT, VEC>(P, s, a, tt, ntiles);
 }
 
+// Whole draw from a filtered row whose kept logits are listed (n <= one per
+// thread): r at the listed tokens (r is 0 off the list, where p is 0), put
+// in vocabulary order by rank, then the inverse CDF of locate_token over
+// those n values. Returns the token, or -1 if r has no mass.
+template <int DT>
+__device__ int draw_list(const Params& P, Smem& s, const DrawArgs& a, const int2* ent, int n) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // Scratch in the tile-sum area, idle outside a streamed draw.
+  int* lx = reinterpret_cast<int*>(s.wtot);  // [n] listed tokens
+  int* ox = lx + kThreads;                   // [n] tokens in vocabulary order
+  float* orr = s.wtot + 2 * kThreads;        // [n] r in vocabulary order
+  int x = INT_MAX;
+  float r = 0.f;
+  if (tid < n) {
+    const int2 e = __ldcg(ent + tid);
+    x = e.x;
+    const float ep = ex2(fmaf(__int_as_float(e.y), P.c, -a.mcp));
+    if (a.kind == kResidual) {
+      const float zq = mask_below<DT>(Elem<DT & 1>::scalar(a.drow, x), a.tau_q);
+      const float eq = ex2(fmaf(zq, P.c, -a.mcq));
+      float d = fmaf(-eq, a.bhi, ep);
+      d = fmaf(-eq, a.blo, d);
+      r = fmaxf(d, 0.f);
+    } else {
+      r = (a.kind == kOneHot && x == a.xhat) ? 0.f : ep;
+    }
+    lx[tid] = x;
+  }
+  if (tid == 0) s.pick = -1;
+  __syncthreads();
+  if (tid < n) {
+    int rank = 0;  // tokens are distinct
+    for (int j = 0; j < n; ++j) rank += lx[j] < x ? 1 : 0;
+    ox[rank] = x;
+    orr[rank] = r;
+  }
+  __syncthreads();
+  const double rv = tid < n ? (double)orr[tid] : 0.0;
+  const double inc = warp_incl_scan_d(rv, lane);
+  if (lane == 31) s.dred[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    double v = lane < kWarps ? s.dred[lane] : 0.0;
+    v = warp_incl_scan_d(v, lane);
+    if (lane < kWarps) s.dred2[lane] = v;
+  }
+  __syncthreads();
+  double lo = __shfl_up_sync(kFull, inc, 1);
+  if (lane == 0) lo = 0.0;
+  lo += warp ? s.dred2[warp - 1] : 0.0;
+  const double Z = s.dred2[kWarps - 1];
+  int y = -1;
+  if (Z > 0.0) {
+    double T = a.u2 * Z;
+    if (!(T >= 0.0)) T = 0.0;  // a NaN or negative uniform draws the first token with mass
+    if (tid < n && rv > 0.0 && lo <= T) atomicMax(&s.pick, tid);
+    __syncthreads();
+    y = s.pick >= 0 ? ox[s.pick] : -1;
+  }
+  __syncthreads();  // the scratch is free again
+  return y;
+}
+
 // Writes the drawn token and (p(y), q(y)) (thread 0).
 template <int DT>
 __device__ void finish_draw(const Params& P, const DrawArgs& a, double Sp, double Sq, int y,
@@ -1112,6 +1177,33 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
   }
   const double Sp = __ldcg(&P.rows[srow].S_p), Sq = __ldcg(&P.rows[srow].S_q);
   const float mcp = __ldcg(&P.rows[srow].mc_p), mcq = __ldcg(&P.rows[srow].mc_q);
+  if constexpr (VEC && (DT & kFilt) != 0) {
+    // A filtered stop row with its kept logits listed: the draw reads the
+    // list (and the draft row at the listed tokens), not the rows.
+    const int nl = P.flist ? __ldcg(&P.fst[srow].nl) : 0;
+    if (nl > 0 && nl <= kThreads) {
+      if (tid == 0) atomicAdd(&P.ws->committed, 1u);
+      const DrawArgs a = make_draw_args(P, (size_t)P.V * Elem<DT & 1>::kBytes, srow, drow, kind, xhat,
+                                        mcp, mcq, Sp, Sq);
+      const int2* ent = P.flist + (size_t)srow * kKeptListCap;
+      int y = draw_list<DT>(P, s, a, ent, nl);
+      if (y < 0 && kind != kBonus) {
+        // No residual mass (p == q in fp32): draw from p instead.
+        if (tid == 0) atomicOr(&P.ws->status, SV_DATA_DEGENERATE_RESIDUAL);
+        DrawArgs used = a;
+        used.kind = kBonus;
+        used.bhi = 1.f;
+        used.blo = 0.f;
+        y = draw_list<DT>(P, s, used, ent, nl);
+      }
+      if (y < 0) {
+        if (tid == 0) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
+        y = 0;
+      }
+      if (tid == 0) finish_draw<DT>(P, a, Sp, Sq, y, t0 + K);
+      return true;
+    }
+  }
   if (VEC && kind == kBonus && (__ldcg(&P.rows[srow].accept) & 2u)) {
     // The bonus row left its tile sums: only the chosen tile is read again.
     if (tid == 0) atomicAdd(&P.ws->committed, 1u);
@@ -1621,7 +1713,9 @@ __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int 
     if (part < 0 && P.fst) {
       if (tid == 0) {
         const FStat ft = P.fst[t];
-        const FStat fd = has_d ? P.fst_d[d0 + i] : FStat{0.f, 1, 0.0};
+        FStat fd{};
+        fd.ok = 1;
+        if (has_d) fd = P.fst_d[d0 + i];
         int ok = !greedy && ft.ok && fd.ok;
         if (ok) {
           st.mc_p = ft.mc;
@@ -1915,7 +2009,7 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
                             void* workspace, size_t workspace_bytes, void* stream,
                             int greedy_all, const float* thr = nullptr,
                             const float* thr_d = nullptr, const FStat* fst = nullptr,
-                            const FStat* fst_d = nullptr) {
+                            const FStat* fst_d = nullptr, const int2* flist = nullptr) {
   const sv_status chk = check_verify_args(target, draft, dtype, V, B, draft_tokens, cu_draft, uniforms,
                                           temperature, out_tokens, out_len, out_probs, greedy_all);
   if (chk != SV_OK || B == 0) return chk;
@@ -1955,6 +2049,7 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
   P.thr_d = thr_d;
   P.fst = fst;
   P.fst_d = fst_d;
+  P.flist = flist;
 
   // Bulk copies need 16-byte aligned row starts and 16-byte multiples.
   const bool vec = ((uintptr_t)target % 16 == 0) && (!P.draft || (uintptr_t)P.draft % 16 == 0) &&
@@ -2038,8 +2133,12 @@ sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logit
 static size_t filter_thr_bytes(int64_t R_t, int64_t B) {
   return sv::align16((size_t)R_t * 4) + sv::align16((size_t)(R_t - B) * 4 + 4);
 }
+static size_t filter_fst_bytes(int64_t R_t, int64_t B) {
+  return (size_t)R_t * sizeof(sv::FStat) + (size_t)(R_t - B + 1) * sizeof(sv::FStat);
+}
 static size_t filter_bytes(int64_t R_t, int64_t B) {
-  return filter_thr_bytes(R_t, B) + (size_t)R_t * sizeof(sv::FStat) + (size_t)(R_t - B + 1) * sizeof(sv::FStat);
+  return filter_thr_bytes(R_t, B) + filter_fst_bytes(R_t, B) +
+         (size_t)R_t * sv::kKeptListCap * sizeof(int2);
 }
 
 size_t spec_verify_filtered_workspace_size(int32_t B, int32_t R_t, int32_t V) {
@@ -2088,12 +2187,14 @@ sv_status spec_verify_filtered(const void* target_logits, const void* draft_logi
   fp.thr_d = reinterpret_cast<float*>(ws + sv::align16((size_t)R_t * 4));
   fp.fst_t = reinterpret_cast<sv::FStat*>(ws + filter_thr_bytes(R_t, B));
   fp.fst_d = fp.fst_t + R_t;
+  fp.list_t = reinterpret_cast<int2*>(ws + filter_thr_bytes(R_t, B) + filter_fst_bytes(R_t, B));
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   if (sv::launch_thresholds(fp, dtype, st) != cudaSuccess) return SV_ERR_CUDA;
   return sv::run_verify(target_logits, draft_logits, dtype, V, B, draft_tokens, cu_draft, mode,
                         uniforms, temperature, out_tokens, out_len, out_probs, ws + fb,
                         workspace_bytes - fb, cuda_stream, 0, fp.thr_t,
-                        draft_logits ? fp.thr_d : nullptr, fp.fst_t, draft_logits ? fp.fst_d : nullptr);
+                        draft_logits ? fp.thr_d : nullptr, fp.fst_t, draft_logits ? fp.fst_d : nullptr,
+                        fp.list_t);
 }
 
 size_t spec_verify_workspace_size(int32_t B, int32_t R_t, int32_t V) {

@@ -11,12 +11,21 @@ namespace sv {
 // its buffer held every kept logit of the row (ok = 1): mc = fp32(M * c) for
 // the row maximum M, and S = sum over the kept logits z of 2^(z c - mc).
 // ok = 0: the verify kernel computes them from the row.
+// nl > 0: the row's kept logits are also listed, nl entries (token, logit)
+// in the row's block of the kept lists, so that a draw from the row reads
+// the list instead of the row. nl = 0: no list.
 struct alignas(16) FStat {
   float mc;
   int ok;
   double S;
+  int nl;
+  int unused[3];
 };
-static_assert(sizeof(FStat) == 16, "filtered row statistics are 16 bytes");
+static_assert(sizeof(FStat) == 32, "filtered row statistics are 32 bytes");
+
+// Entries of a kept list per target row, at most; more kept logits (ties at
+// the threshold) leave no list.
+constexpr int kKeptListCap = 256;
 
 struct FtParams {
   const void* target;   // [R_t, V]
@@ -33,6 +42,7 @@ struct FtParams {
   float* thr_d;         // [rows_t - B]
   FStat* fst_t;         // [rows_t] filtered statistics of the target rows, or NULL
   FStat* fst_d;         // [rows_t - B] of the draft rows, or NULL
+  int2* list_t;         // [rows_t, kKeptListCap] kept (token, logit bits) of the target rows, or NULL
   bool after_warp;      // the one-warp-per-row kernel ran first: skip the rows it finished
 };
 

@@ -207,3 +207,44 @@ def test_warp_rows_and_fallback_rows_in_one_batch(cuda_lib, dtype, top_k, top_p)
         b.target, b.draft = zt, zd
     rep = _run(b, top_k, top_p)
     assert rep.mismatched_requests <= 1
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_listed_rows_degenerate_residual_and_one_hot(cuda_lib, dtype):
+    """Top-k rows the one-warp kernel lists: their draws read the kept list.
+    The draft rows equal the target rows and the proposals are tokens of
+    no mass under q' (outside the top k), so every request rejects its first
+    proposal with certainty and the residual max(0, p' - q') is empty: the
+    draw falls back to p' and the status word says so. The same batch with
+    one-hot proposals removes x̂ from p' instead."""
+    rng = np.random.default_rng(580)
+    V, k = 32000, 40
+    b = W.gaussian_sampling(seed=581, B=24, K=4, V=V, sigma=2.0, draft_sigma=0.5, T=0.8, dtype=dtype)
+    rows_d = np.concatenate([np.arange(b.cu_draft[i] + i, b.cu_draft[i + 1] + i) for i in range(b.B)])
+    b.draft = b.target[rows_d].copy()
+    zt = W.bf16_bits_to_f32(b.target) if dtype == "bf16" else b.target
+    zd = zt[rows_d]
+    # Proposals below every row's k-th largest logit: q'(x̂) = 0.
+    kth = -np.sort(-zd, axis=1)[:, k - 1]
+    prop = np.empty(rows_d.size, np.int32)
+    for j in range(rows_d.size):
+        cand = np.nonzero(zd[j] < kth[j])[0]
+        prop[j] = cand[rng.integers(cand.size)]
+    b.draft_tokens = prop
+    db = parity.to_device(b)
+    nbytes = api.spec_verify_filtered_workspace_size(b.B, b.R_t, b.V)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    tok, ln, pr = api.spec_verify_filtered(db.target, db.draft, db.draft_tokens, db.cu_draft, db.uniforms,
+                                           db.temperature, k, 1.0, db.mode, workspace=ws)
+    torch.cuda.synchronize()
+    fb = nbytes - api.spec_verify_workspace_size(b.B, b.R_t, b.V)
+    assert api.sv_check_status(ws[fb:]) == api.SV_DATA_DEGENERATE_RESIDUAL
+    assert (ln.cpu().numpy() == 1).all()
+    import oracle
+    ora = oracle.spec_verify(b.target, b.draft, b.draft_tokens, b.cu_draft, b.uniforms, b.temperature, b.mode,
+                             top_k=k, top_p=1.0)
+    rep = parity.compare(b, (tok.cpu().numpy(), ln.cpu().numpy(), pr.cpu().numpy()), ora)
+    assert rep.mismatched_requests == 0, rep.as_dict()
+    b.draft = None
+    rep = _run(b, k, 1.0)
+    assert rep.mismatched_requests == 0, rep.as_dict()
