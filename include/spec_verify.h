@@ -158,6 +158,33 @@ sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype, int32_t 
                              size_t workspace_bytes, void* cuda_stream);
 
 /*
+ * Which kernel runs spec_verify and spec_verify_greedy. Both compute the
+ * same step (the rule above):
+ *   - a persistent kernel, a fixed number of CTAs per SM, streams rows
+ *     through a shared-memory ring and commits each request as soon as its
+ *     stop slot is known; the default for large batches;
+ *   - a cluster kernel, one thread-block cluster of 8 CTAs per target row:
+ *     the row (and its paired draft row) is held in the CTAs' shared memory,
+ *     the slices' statistics are exchanged through distributed shared
+ *     memory, every rejecting row (and every bonus row) draws its token at
+ *     once, and each request's last row to finish commits it. For batches of
+ *     few rows, where the persistent kernel's time is a chain of dependent
+ *     steps rather than bytes.
+ * The cluster kernel runs when the workspace holds at most `rows` target
+ * rows ((workspace_bytes - spec_verify_workspace_size(B, 0, V)) / 32 <=
+ * rows; a workspace sized for R_t holds R_t), the rows are 16-byte aligned
+ * with V * element size a multiple of 16, and a row pair fits 200 KB of
+ * shared memory per CTA (V * element size <= 800 KB with draft rows, 1.6 MB
+ * without). The filtered and no-allocation entry points always take the
+ * persistent kernel.
+ * Sets the process-wide threshold (0: never) and returns the previous one;
+ * the initial value is SV_CLUSTER_ROWS_DEFAULT. Negative values are ignored
+ * (the call then only returns the current threshold).
+ */
+#define SV_CLUSTER_ROWS_DEFAULT 64
+int32_t sv_set_cluster_rows(int32_t rows);
+
+/*
  * Top-k / top-p filtered verify-and-commit ("投机解码从零实现", §5.4
  * "采样策略对比": top-k and nucleus rejection sampling keep the output
  * distribution when the same filter is applied to the target and the draft

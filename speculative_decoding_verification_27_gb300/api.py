@@ -422,6 +422,16 @@ def spec_verify_filtered(target: torch.Tensor, draft: Optional[torch.Tensor], dr
     return out_tokens, out_len, out_probs
 
 
+def sv_set_cluster_rows(rows: int) -> int:
+    """Largest workspace (in target rows) that spec_verify runs with the
+    cluster kernel (0: never; negative: only read); returns the previous
+    threshold. Process-wide."""
+    lib = load()
+    lib.sv_set_cluster_rows.argtypes = [ctypes.c_int32]
+    lib.sv_set_cluster_rows.restype = ctypes.c_int32
+    return int(lib.sv_set_cluster_rows(int(rows)))
+
+
 SV_SELECT_UNIFORM, SV_SELECT_LONGEST_BIASED = 0, 1
 
 

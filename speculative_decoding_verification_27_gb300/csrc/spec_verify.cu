@@ -42,6 +42,7 @@
 #include "../../include/spec_verify.h"
 #include "sv_device.cuh"
 #include "sv_filter.cuh"
+#include "sv_cluster.cuh"
 
 namespace sv {
 
@@ -200,6 +201,7 @@ struct Params {
   RowRec* rows;             // [R_t]
   long long row_cap;
   int greedy_all;
+  int may_publish;          // some draw of this call may be published in parts
 };
 
 struct Smem {
@@ -1839,7 +1841,10 @@ __global__ void __launch_bounds__(kThreads, SV_MINBLOCKS) verify_kernel(Params P
       if (t < n_items) {
         s.wk = 2;
         s.item = (int)t;
-      } else {
+      } else if (P.may_publish) {
+        // Rows are all handed out: stay for parts of draws published later
+        // (none can be when every draw is too small to split or the batch
+        // is greedy; then leave at once).
         for (unsigned poll = 0; poll < kLingerPolls; ++poll) {
           if (claim_draw_part(P, slot, part)) {
             s.wk = 1;
@@ -2002,6 +2007,9 @@ static sv_status check_verify_args(const void* target, const void* draft, sv_dty
   return SV_OK;
 }
 
+// Workspaces holding at most this many target rows take the cluster kernel.
+static std::atomic<int> g_cluster_rows{SV_CLUSTER_ROWS_DEFAULT};
+
 static sv_status run_verify(const void* target, const void* draft, sv_dtype dtype, int32_t V,
                             int32_t B, const int32_t* draft_tokens, const int32_t* cu_draft,
                             const uint8_t* mode, const float* uniforms, float temperature,
@@ -2045,6 +2053,8 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
   P.rows = reinterpret_cast<RowRec*>(ws + L.rows);
   P.row_cap = (long long)((workspace_bytes - L.rows) / sizeof(RowRec));
   P.greedy_all = greedy_all;
+  // Draws are published in parts only if they stream kMinPublishBytes or more.
+  P.may_publish = !greedy_all && (size_t)V * es * (P.draft ? 2 : 1) >= kMinPublishBytes;
   P.thr = thr;
   P.thr_d = thr_d;
   P.fst = fst;
@@ -2056,6 +2066,31 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
                    (((size_t)V * es) % 16 == 0);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (vec && !thr && P.row_cap <= (long long)g_cluster_rows.load(std::memory_order_relaxed) &&
+      cluster_smem_bytes((size_t)V * es, P.draft != nullptr) > 0) {
+    CParams C;
+    C.target = target;
+    C.draft = P.draft;
+    C.V = V;
+    C.B = B;
+    C.draft_tokens = draft_tokens;
+    C.cu = cu_draft;
+    C.mode = P.mode;
+    C.uniforms = uniforms;
+    C.c = P.c;
+    C.out_tokens = out_tokens;
+    C.out_len = out_len;
+    C.out_probs = P.out_probs;
+    C.status = &P.ws->status;
+    C.arrive = P.req_state;
+    C.rows = reinterpret_cast<CRow*>(P.rows);
+    C.row_cap = P.row_cap;
+    C.greedy_all = greedy_all;
+    C.nvec = (int)(((size_t)V * es) / 16);
+    C.vp = 0;
+    e = launch_cluster_verify(C, dtype == SV_BF16 ? 1 : 0, st);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  }
   if (thr) {
     if (dtype == SV_BF16)
       e = vec ? launch<1 | kFilt, true>(P, st) : launch<1 | kFilt, false>(P, st);
@@ -2245,6 +2280,11 @@ const char* sv_status_string(sv_status status) {
     case SV_ERR_DATA: return "SV_ERR_DATA";
   }
   return "SV_ERR_UNKNOWN";
+}
+
+int32_t sv_set_cluster_rows(int32_t rows) {
+  if (rows < 0) return sv::g_cluster_rows.load();
+  return sv::g_cluster_rows.exchange(rows);
 }
 
 }  // extern "C"

@@ -287,6 +287,29 @@ __device__ __forceinline__ DF df_mul_f(DF a, float f) {
   return {hi, lo};
 }
 
+__device__ __forceinline__ DF df_neg(DF a) { return {-a.hi, -a.lo}; }
+__device__ __forceinline__ DF df_sub(DF a, DF b) { return df_add(a, df_neg(b)); }
+
+// a <= b for normalised pairs (|lo| <= ulp(hi) / 2).
+__device__ __forceinline__ bool df_le(DF a, DF b) { return a.hi < b.hi || (a.hi == b.hi && a.lo <= b.lo); }
+__device__ __forceinline__ bool df_pos(DF a) { return a.hi > 0.f || (a.hi == 0.f && a.lo > 0.f); }
+
+// a / b to about 2^-44 relative: a quotient in fp32, then its correction
+// from the exact remainder (one more fp32 division). b must be nonzero.
+__device__ __forceinline__ DF df_div(DF a, DF b) {
+  const float q1 = __fdiv_rn(a.hi, b.hi);
+  // remainder a - q1 * b, with q1 * b.hi split exactly
+  const float p = q1 * b.hi;
+  const float pe = fmaf(q1, b.hi, -p);
+  DF r = df_sub(a, DF{p, pe});
+  r = df_add_f(r, -q1 * b.lo);
+  const float q2 = __fdiv_rn(r.hi, b.hi);
+  const float hi = q1 + q2;
+  return {hi, q2 - (hi - q1)};
+}
+
+__device__ __forceinline__ double df_to_d(DF a) { return (double)a.hi + (double)a.lo; }
+
 // ---------------------------------------------------------------------------
 // Warp / CTA reductions (kThreads threads, all participating)
 // ---------------------------------------------------------------------------
@@ -328,6 +351,16 @@ __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
   for (int o = 1; o < 32; o <<= 1) {
     float u = __shfl_up_sync(kFull, v, o);
     if (lane >= o) v += u;
+  }
+  return v;
+}
+
+// The same scan in double-float.
+__device__ __forceinline__ DF warp_incl_scan_df(DF v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF u{__shfl_up_sync(kFull, v.hi, o), __shfl_up_sync(kFull, v.lo, o)};
+    if (lane >= o) v = df_add(u, v);
   }
   return v;
 }

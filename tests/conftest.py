@@ -32,3 +32,15 @@ def cuda_lib():
     from speculative_decoding_verification_27_gb300 import api, build
     build.build_library()
     return api.load()
+
+
+@pytest.fixture(params=["persistent", "cluster"])
+def kernel_path(request, cuda_lib):
+    """Runs the test once with each verify kernel: the persistent kernel
+    (cluster threshold 0) and the one-cluster-per-row kernel (threshold above
+    any test's rows; rows that are not 16-byte vectors still take the
+    persistent kernel). The threshold is restored afterwards."""
+    from speculative_decoding_verification_27_gb300 import api
+    prev = api.sv_set_cluster_rows(0 if request.param == "persistent" else 1 << 20)
+    yield request.param
+    api.sv_set_cluster_rows(prev)

@@ -23,7 +23,7 @@ def _run(batch, workspace=None, flag_budget=None, draw_flags_in_budget=True):
 # --------------------------------------------------------------------------
 # The five configurations
 # --------------------------------------------------------------------------
-def test_config1_sampling_1000_rounds(cuda_lib):
+def test_config1_sampling_1000_rounds(cuda_lib, kernel_path):
     """B=1, K=4, V=32000 fp32, T=1: 1000 rounds of fresh logits, one workspace."""
     ws = api.new_workspace(1, 5, 32000)
     total = parity.ParityReport(0, 0, 0, 0, 0, 0.0, 0)
@@ -39,7 +39,7 @@ def test_config1_sampling_1000_rounds(cuda_lib):
     assert api.sv_check_status(ws) == 0
 
 
-def test_config2_greedy_full_bit_exact(cuda_lib):
+def test_config2_greedy_full_bit_exact(cuda_lib, kernel_path):
     b = W.config2(seed=102)
     db = parity.to_device(b)
     tok, ln = api.spec_verify_greedy(db.target, db.draft_tokens, db.cu_draft)
@@ -58,7 +58,7 @@ def test_config2_greedy_full_bit_exact(cuda_lib):
     assert rep.mismatched_requests == 0 and rep.flagged_requests == 0
 
 
-def test_config3_sampling_full(cuda_lib):
+def test_config3_sampling_full(cuda_lib, kernel_path):
     """B=256, K=7, V=151936 bf16, T=0.7 (the benchmark's workload), every request."""
     rep, _, _ = _run(W.config3(seed=103), flag_budget=parity.FLAG_BUDGET)
     print("config3:", rep.as_dict())
@@ -72,7 +72,7 @@ def test_config3_literal_zipf_reading(cuda_lib):
     assert rep.mismatched_requests <= max(1, 1e-4 * rep.rows)
 
 
-def test_config4_ngram_then_one_hot_verify(cuda_lib):
+def test_config4_ngram_then_one_hot_verify(cuda_lib, kernel_path):
     import oracle
     nb = W.config4_histories(seed=104)
     h = torch.from_numpy(nb.histories).cuda()
@@ -95,7 +95,7 @@ def test_config4_ngram_then_one_hot_verify(cuda_lib):
     assert rep.mismatched_requests <= max(1, 1e-4 * rep.rows)
 
 
-def test_config5_ragged_mixed_full(cuda_lib):
+def test_config5_ragged_mixed_full(cuda_lib, kernel_path):
     """B=512, K_b in 1..8, V=256000 bf16, half greedy requests."""
     rep, _, _ = _run(W.config5(seed=105), flag_budget=parity.FLAG_BUDGET, draw_flags_in_budget=False)  # flat rows
     print("config5:", rep.as_dict())
@@ -107,7 +107,7 @@ def test_config5_ragged_mixed_full(cuda_lib):
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
 @pytest.mark.parametrize("V", [1, 2, 3, 7, 33, 1000, 4097, 8200])
-def test_small_and_ragged_vocab(cuda_lib, dtype, V):
+def test_small_and_ragged_vocab(cuda_lib, kernel_path, dtype, V):
     """V not a multiple of the vector width takes the scalar-load path."""
     Ks = np.array([0, 1, 3, 5, 2, 0, 4], np.int32)
     b = W.gaussian_sampling(seed=200 + V, B=Ks.size, K=Ks, V=V, sigma=2.0, draft_sigma=0.7,
@@ -118,13 +118,13 @@ def test_small_and_ragged_vocab(cuda_lib, dtype, V):
 
 
 @pytest.mark.parametrize("T", [0.3, 1.0, 2.5])
-def test_temperatures(cuda_lib, T):
+def test_temperatures(cuda_lib, kernel_path, T):
     b = W.gaussian_sampling(seed=300, B=40, K=5, V=5000, sigma=3.0, draft_sigma=1.0, T=T, dtype="bf16")
     rep, _, _ = _run(b)
     assert rep.mismatched_requests <= 1
 
 
-def test_one_hot_proposals(cuda_lib):
+def test_one_hot_proposals(cuda_lib, kernel_path):
     b = W.gaussian_sampling(seed=301, B=64, K=4, V=3000, sigma=1.0, draft_sigma=0.5, T=1.0)
     b.draft = None
     rep, _, _ = _run(b)
@@ -143,7 +143,7 @@ def test_unaligned_rows_take_scalar_path(cuda_lib):
     parity.compare(b, gpu, parity.oracle_verify(b))
 
 
-def test_masked_logits_and_ties(cuda_lib):
+def test_masked_logits_and_ties(cuda_lib, kernel_path):
     V = 64
     zt = np.full((6, V), -np.inf, np.float32)
     zt[:, 5] = 1.0
@@ -169,7 +169,7 @@ def test_empty_batch_is_a_noop(cuda_lib):
     assert ln.numel() == 0
 
 
-def test_rerun_is_bit_identical(cuda_lib):
+def test_rerun_is_bit_identical(cuda_lib, kernel_path):
     b = W.config5(seed=303, B=48, V=20000)
     db = parity.to_device(b)
     a = parity.gpu_verify(db)
@@ -178,7 +178,7 @@ def test_rerun_is_bit_identical(cuda_lib):
         assert np.array_equal(x, y)
 
 
-def test_data_errors_set_status_and_leave_workspace_usable(cuda_lib):
+def test_data_errors_set_status_and_leave_workspace_usable(cuda_lib, kernel_path):
     b = W.gaussian_sampling(seed=304, B=8, K=3, V=512, sigma=1.0, draft_sigma=0.5, T=1.0)
     ws = api.new_workspace(b.B, b.R_t, b.V)
     db = parity.to_device(b)
@@ -198,7 +198,7 @@ def test_data_errors_set_status_and_leave_workspace_usable(cuda_lib):
 # --------------------------------------------------------------------------
 # Statistics of the GPU path itself
 # --------------------------------------------------------------------------
-def test_chi_square_through_the_gpu(cuda_lib):
+def test_chi_square_through_the_gpu(cuda_lib, kernel_path):
     """1e6 rounds, V=16, K=1: the first emitted token follows p (lossless)."""
     from scipy.special import softmax
     rng = np.random.default_rng(12)
@@ -304,3 +304,39 @@ def test_default_workspace_is_reused_without_clearing(cuda_lib):
     assert api.default_workspace_clears == clears + 2
     assert api.default_workspace(0, "cuda", layout=("verify", a.B, a.V)).data_ptr() == ws.data_ptr()
     assert api.sv_check_status(ws) == 0
+
+
+# --------------------------------------------------------------------------
+# Kernel choice
+# --------------------------------------------------------------------------
+def test_cluster_threshold_default_and_dispatch(cuda_lib):
+    """spec_verify takes the one-cluster-per-row kernel when the workspace
+    holds at most SV_CLUSTER_ROWS_DEFAULT = 64 target rows; both kernels give
+    the oracle's commits on a batch right at the threshold and past it."""
+    assert api.sv_set_cluster_rows(-1) == 64
+    for B in (16, 17):  # K = 3: 64 and 68 target rows
+        b = W.gaussian_sampling(seed=700 + B, B=B, K=3, V=4096, sigma=2.0, draft_sigma=0.7, T=0.9, dtype="bf16")
+        rep, _, _ = _run(b)
+        assert rep.mismatched_requests <= 1
+
+
+def test_cluster_rows_beyond_the_workspace_are_reported(cuda_lib):
+    """Offsets that claim more rows than the workspace holds: the cluster
+    kernel sets SV_DATA_BAD_OFFSETS and writes no output."""
+    prev = api.sv_set_cluster_rows(1 << 20)
+    try:
+        b = W.gaussian_sampling(seed=720, B=4, K=3, V=512, sigma=1.0, draft_sigma=0.5, T=1.0)
+        db = parity.to_device(b)
+        ws = api.new_workspace(b.B, b.R_t, b.V)
+        cu_bad = db.cu_draft.clone()
+        cu_bad[-1] += 3  # R_t beyond the workspace (and beyond the caller's rows: nothing may read them)
+        ln = torch.full((b.B,), -7, dtype=torch.int32, device="cuda")
+        api.spec_verify(db.target, db.draft, db.draft_tokens, cu_bad, db.uniforms, 1.0, out_len=ln, workspace=ws)
+        torch.cuda.synchronize()
+        assert api.sv_check_status(ws) & api.SV_DATA_BAD_OFFSETS
+        assert (ln.cpu().numpy() == -7).all()
+        gpu = parity.gpu_verify(db, ws)
+        parity.compare(b, gpu, parity.oracle_verify(b))
+        assert api.sv_check_status(ws) == 0
+    finally:
+        api.sv_set_cluster_rows(prev)
