@@ -8,9 +8,12 @@
 //      a ring of shared-memory stages filled by bulk asynchronous copies (the
 //      TMA engine), and keeps a single-pass online softmax: per thread a running
 //      maximum and one fp32 partial sum per vector lane, rescaled when the
-//      maximum grows. Sums are combined in double-float arithmetic, so
-//      S = sum_x 2^(z_x c - Mc) (c = log2(e)/T, Mc = fp32(max z * c)) is
-//      accurate to ~1e-9 relative. Greedy rows compute the argmax instead
+//      maximum grows. Sums are combined, kept and scanned in double-float
+//      arithmetic (fp32 pairs), so S = sum_x 2^(z_x c - Mc) (c = log2(e)/T,
+//      Mc = fp32(max z * c)) is accurate to ~1e-9 relative. No fp64 sits on
+//      a dependent path: on this part a dependent fp64 operation takes about
+//      14 times as long as an fp32 one, and a division about 6 times as long
+//      as an fp32 division. Greedy rows compute the argmax instead
 //      (lowest index among ties). The CTA then gathers z[x̂] and decides the
 //      slot: accept iff u < min(1, p(x̂)/q(x̂)) ("Draft Model（草稿模型）", §2
 //      "接受-拒绝准则"; a zero draft probability rejects, "投机解码从零实现"
@@ -61,8 +64,8 @@ static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
 struct alignas(16) RowRec {
   float mc_p;        // fp32(max z_target * c): exponent offset of the target row
   float mc_q;        // same for the paired draft row (sampled draft slots)
-  double S_p;        // sum_x 2^(z_x c - mc_p) over the target row
-  double S_q;        // same over the draft row
+  DF S_p;            // sum_x 2^(z_x c - mc_p) over the target row (double-float)
+  DF S_q;            // same over the draft row
   int argmax;        // greedy rows: first index of the maximum
   unsigned accept;   // bit 0: the slot's draft token is accepted; bit 1 (bonus
                      // rows): the tile sums of r = 2^(z c - mc_p) are stored
@@ -73,7 +76,7 @@ static_assert(sizeof(RowRec) == 32, "row record is 32 bytes");
 // RowRec over the part's slice, S = 0 for a slice without a finite logit.
 struct alignas(16) PartRec {
   float mc_p, mc_q;
-  double S_p, S_q;
+  DF S_p, S_q;
   float amax_v;      // greedy: largest logit of the slice
   int amax_i;        // and its first index (0x7fffffff if none)
 };
@@ -93,7 +96,7 @@ struct alignas(16) DrawDesc {
   int xhat;         // the rejected one-hot proposal, or -1
   float mcp, mcq;   // exponent offsets of the stop rows
   int nparts;       // parts the draw is split into
-  double Sp, Sq;    // sums of the stop rows
+  DF Sp, Sq;        // sums of the stop rows
   unsigned unused;
   unsigned done;    // parts finished
   int bonus_row;    // row that receives (p(y), q(y)) of the drawn token
@@ -188,8 +191,8 @@ struct Params {
   unsigned long long* req_state;  // [B] rows finished (and accepted) per request
   unsigned int* slot_state; // [n_slots] nparts << 20 | parts handed out (0: unpublished)
   DrawDesc* descs;          // [n_slots]
-  double* tsum;             // [n_slots, tsum_stride] per-tile sums of r
-  double* btile;            // [B, tsum_stride] tile sums of a bonus row's r = S_p p
+  DF* tsum;                 // [n_slots, tsum_stride] per-tile sums of r
+  DF* btile;                // [B, tsum_stride] tile sums of a bonus row's r = S_p p
   const float* thr;         // [R_t] filter thresholds of the target rows, or NULL
   const float* thr_d;       // [R_d] filter thresholds of the draft rows, or NULL
   const FStat* fst;         // [R_t] filtered softmax statistics of the target rows, or NULL
@@ -222,10 +225,10 @@ struct Smem {
   DF reddf_p[kWarps];
   DF reddf_q[kWarps];
   float bcast_f[2];
-  double dred[kWarps];
-  double dred2[kWarps];
-  double wexcl[kWarps + 1];
-  double tincl[kMaxScanTiles];
+  DF dred[kWarps];
+  DF dred2[kWarps];
+  DF wexcl[kWarps + 1];
+  DF tincl[kMaxScanTiles];
   float wtot[kMaxScanTiles * kWarps];
 };
 
@@ -639,7 +642,7 @@ __device__ __forceinline__ void argmax_scalar(const void* trow, int V, float& bv
 // and, if has_d, the draft row. Results are valid in thread 0.
 template <int EPV>
 __device__ void combine_softmax(SoftAcc<EPV>& at, SoftAcc<EPV>& ad, bool has_d, float c, Smem& s,
-                                float& Mc_p, double& S_p, float& Mc_q, double& S_q) {
+                                float& Mc_p, DF& S_p, float& Mc_q, DF& S_q) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float mp = warp_max(at.m);
   float mq = has_d ? warp_max(ad.m) : -INFINITY;
@@ -686,38 +689,28 @@ __device__ void combine_softmax(SoftAcc<EPV>& at, SoftAcc<EPV>& ad, bool has_d, 
     if (lane == 0) {
       Mc_p = mcp;
       Mc_q = mcq;
-      S_p = (double)v.hi + (double)v.lo;
-      S_q = (double)w.hi + (double)w.lo;
+      S_p = v;
+      S_q = w;
     }
   }
 }
 
-// The same search by a whole warp: each round tests 32 evenly spaced
-// candidates of the remaining range at once (cu[b] + b increases with b, so
-// the candidates that pass form a prefix), two rounds up to B = 1024.
-__device__ __forceinline__ int find_request_warp(const int32_t* cu, int B, int t, int lane) {
-  int lo = 0, n = B;  // the answer lies in [lo, lo + n); cu[lo] + lo <= t
+// Largest b in [0, B) with cu[b] (+ b when plus_b) <= j: the request that
+// owns target row j (plus_b) or draft slot j. The keys do not decrease with
+// b and key(0) = 0 <= j. Every thread of the CTA calls it: each round tests
+// kThreads evenly spaced candidates of the remaining range at once, and the
+// candidates that pass form a prefix whose length one barrier counts. One
+// round (one memory round trip) up to B = kThreads, two up to kThreads^2.
+__device__ __forceinline__ int find_request_cta(const int32_t* cu, int B, int j, bool plus_b) {
+  int lo = 0, n = B;  // the answer lies in [lo, lo + n); key(lo) <= j
   while (n > 1) {
-    const int step = (n + 31) >> 5;
-    const int c = lo + lane * step;
-    const bool pass = c < lo + n && cu[c] + c <= t;
-    const unsigned m = __ballot_sync(kFull, pass);
-    const int k = 31 - __clz(m);  // lane 0 (candidate lo) always passes
+    const int step = (n + kThreads - 1) / kThreads;
+    const int c = lo + (int)threadIdx.x * step;
+    const bool pass = c < lo + n && cu[c] + (plus_b ? c : 0) <= j;
+    const int cnt = __syncthreads_count(pass);  // >= 1: candidate lo passes
     const int end = lo + n;
-    lo += k * step;
+    lo += (cnt - 1) * step;
     n = min(step, end - lo);
-  }
-  return lo;
-}
-
-__device__ __forceinline__ int find_request(const int32_t* cu, int B, int t) {
-  int lo = 0, hi = B - 1;  // largest b with cu[b] + b <= t
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (cu[mid] + mid <= t)
-      lo = mid;
-    else
-      hi = mid - 1;
   }
   return lo;
 }
@@ -732,13 +725,13 @@ struct DrawArgs {
   int row, kind, xhat;
   float mcp, mcq;
   float bhi, blo;    // beta = S_p / S_q as a double-float pair
-  double u2;
+  float u2;
   float tau_p, tau_q;  // filter thresholds of the two rows (-inf: unfiltered)
 };
 
 __device__ __forceinline__ DrawArgs make_draw_args(const Params& P, size_t rowb, int row, int drow,
                                                    int kind, int xhat, float mcp, float mcq,
-                                                   double Sp, double Sq) {
+                                                   DF Sp, DF Sq) {
   DrawArgs a;
   a.row = row;
   a.trow = static_cast<const char*>(P.target) + (size_t)row * rowb;
@@ -747,10 +740,10 @@ __device__ __forceinline__ DrawArgs make_draw_args(const Params& P, size_t rowb,
   a.xhat = xhat;
   a.mcp = mcp;
   a.mcq = mcq;
-  const double beta = kind == kResidual ? Sp / Sq : 1.0;
-  a.bhi = (float)beta;
-  a.blo = (float)(beta - (double)a.bhi);
-  a.u2 = (double)__ldg(&P.uniforms[2 * (size_t)row + 1]);
+  const DF beta = (kind == kResidual && df_pos(Sq)) ? df_div(Sp, Sq) : DF{1.f, 0.f};
+  a.bhi = beta.hi;
+  a.blo = beta.lo;
+  a.u2 = __ldg(&P.uniforms[2 * (size_t)row + 1]);
   a.tau_p = P.thr ? __ldg(&P.thr[row]) : -INFINITY;
   a.tau_q = (P.thr_d && kind == kResidual) ? __ldg(&P.thr_d[drow]) : -INFINITY;
   return a;
@@ -876,35 +869,35 @@ __device__ bool tile_sums(const Params& P, Smem& s, unsigned char* ring, const D
 // mass whose lower edge is <= u' * Z, which is the smallest k whose running
 // sum exceeds u' * Z.
 template <int DT, bool VEC>
-__device__ int locate_token(const Params& P, Smem& s, const DrawArgs& a, double tt, int ntiles) {
+__device__ int locate_token(const Params& P, Smem& s, const DrawArgs& a, DF tt, int ntiles) {
   constexpr int EPV = Elem<DT & 1>::kEPV;
   constexpr int TILE = kThreads * EPV;
   const int V = P.V;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  double inc = warp_incl_scan_d(tt, lane);
+  const DF inc = warp_incl_scan_df(tt, lane);
   if (lane == 31) s.dred[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    double v = lane < kWarps ? s.dred[lane] : 0.0;
-    v = warp_incl_scan_d(v, lane);
+    DF v = lane < kWarps ? s.dred[lane] : DF{0.f, 0.f};
+    v = warp_incl_scan_df(v, lane);
     if (lane < kWarps) s.dred2[lane] = v;
   }
   __syncthreads();
-  if (tid < ntiles) s.tincl[tid] = inc + (warp > 0 ? s.dred2[warp - 1] : 0.0);
+  if (tid < ntiles) s.tincl[tid] = warp > 0 ? df_add(s.dred2[warp - 1], inc) : inc;
   if (tid == 0) s.pick = -1;
   __syncthreads();
-  const double Z = s.tincl[ntiles - 1];
-  if (!(Z > 0.0)) return -1;
-  double T = a.u2 * Z;
-  if (!(T >= 0.0)) T = 0.0;  // a NaN or negative uniform draws the first token with mass
+  const DF Z = s.tincl[ntiles - 1];
+  if (!df_pos(Z)) return -1;
+  DF T = df_mul_f(Z, a.u2);
+  if (!(T.hi >= 0.f)) T = DF{0.f, 0.f};  // a NaN or negative uniform draws the first token with mass
   if (tid < ntiles) {
-    const double lo = tid ? s.tincl[tid - 1] : 0.0;
-    if (tt > 0.0 && lo <= T) atomicMax(&s.pick, tid);
+    const DF lo = tid ? s.tincl[tid - 1] : DF{0.f, 0.f};
+    if (df_pos(tt) && df_le(lo, T)) atomicMax(&s.pick, tid);
   }
   __syncthreads();
   const int kt = s.pick;
   if (kt < 0) return -1;  // unreachable: the first tile with mass has lower edge 0 <= T
-  const double Tk = T - (kt ? s.tincl[kt - 1] : 0.0);
+  const DF Tk = kt ? df_sub(T, s.tincl[kt - 1]) : T;
 
   // The chosen tile: thread k spans [wexcl[w] + lane_lo, wexcl[w] + incl).
   const int x = kt * TILE + tid * EPV;
@@ -925,26 +918,26 @@ __device__ int locate_token(const Params& P, Smem& s, const DrawArgs& a, double 
   if (lane == 31) s.redf[warp] = incl;
   __syncthreads();
   if (tid == 0) {
-    double acc = 0.0;
-    s.wexcl[0] = 0.0;
+    DF acc{0.f, 0.f};
+    s.wexcl[0] = acc;
     for (int w = 0; w < kWarps; ++w) {
-      acc = acc + (double)s.redf[w];
+      acc = df_add_f(acc, s.redf[w]);
       s.wexcl[w + 1] = acc;
     }
     s.pick2 = -1;
     s.tok = -1;
   }
   __syncthreads();
-  const double lo = s.wexcl[warp] + (double)lane_lo;
-  if (ts > 0.f && lo <= Tk) atomicMax(&s.pick2, tid);
+  const DF lo = df_add_f(s.wexcl[warp], lane_lo);
+  if (ts > 0.f && df_le(lo, Tk)) atomicMax(&s.pick2, tid);
   __syncthreads();
   if (tid == s.pick2) {
-    double run = lo;
+    DF run = lo;
     int cand = x;
 #pragma unroll
     for (int j = 0; j < EPV; ++j) {
-      if (r[j] > 0.f && run <= Tk) cand = x + j;
-      run += (double)r[j];
+      if (r[j] > 0.f && df_le(run, Tk)) cand = x + j;
+      run = df_add_f(run, r[j]);
     }
     s.tok = cand;
   }
@@ -959,9 +952,9 @@ __device__ int draw_whole(const Params& P, Smem& s, unsigned char* ring, const D
   constexpr int TILE = kThreads * Elem<DT & 1>::kEPV;
   const int ntiles = (P.V + TILE - 1) / TILE;
   if (!tile_sums<DT, VEC>(P, s, ring, a, 0, ntiles)) return -2;
-  double tt = 0.0;
+  DF tt{0.f, 0.f};
   if (threadIdx.x < ntiles)
-    for (int w = 0; w < kWarps; ++w) tt += (double)s.wtot[threadIdx.x * kWarps + w];
+    for (int w = 0; w < kWarps; ++w) tt = df_add_f(tt, s.wtot[threadIdx.x * kWarps + w]);
   return locate_token<DT, VEC>(P, s, a, tt, ntiles);
 }
 
@@ -1002,25 +995,25 @@ __device__ int draw_list(const Params& P, Smem& s, const DrawArgs& a, const int2
     orr[rank] = r;
   }
   __syncthreads();
-  const double rv = tid < n ? (double)orr[tid] : 0.0;
-  const double inc = warp_incl_scan_d(rv, lane);
+  const float rv = tid < n ? orr[tid] : 0.f;
+  const DF inc = warp_incl_scan_df(DF{rv, 0.f}, lane);
   if (lane == 31) s.dred[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    double v = lane < kWarps ? s.dred[lane] : 0.0;
-    v = warp_incl_scan_d(v, lane);
+    DF v = lane < kWarps ? s.dred[lane] : DF{0.f, 0.f};
+    v = warp_incl_scan_df(v, lane);
     if (lane < kWarps) s.dred2[lane] = v;
   }
   __syncthreads();
-  double lo = __shfl_up_sync(kFull, inc, 1);
-  if (lane == 0) lo = 0.0;
-  lo += warp ? s.dred2[warp - 1] : 0.0;
-  const double Z = s.dred2[kWarps - 1];
+  DF lo{__shfl_up_sync(kFull, inc.hi, 1), __shfl_up_sync(kFull, inc.lo, 1)};
+  if (lane == 0) lo = DF{0.f, 0.f};
+  if (warp) lo = df_add(s.dred2[warp - 1], lo);
+  const DF Z = s.dred2[kWarps - 1];
   int y = -1;
-  if (Z > 0.0) {
-    double T = a.u2 * Z;
-    if (!(T >= 0.0)) T = 0.0;  // a NaN or negative uniform draws the first token with mass
-    if (tid < n && rv > 0.0 && lo <= T) atomicMax(&s.pick, tid);
+  if (df_pos(Z)) {
+    DF T = df_mul_f(Z, a.u2);
+    if (!(T.hi >= 0.f)) T = DF{0.f, 0.f};  // a NaN or negative uniform draws the first token with mass
+    if (tid < n && rv > 0.f && df_le(lo, T)) atomicMax(&s.pick, tid);
     __syncthreads();
     y = s.pick >= 0 ? ox[s.pick] : -1;
   }
@@ -1030,14 +1023,14 @@ __device__ int draw_list(const Params& P, Smem& s, const DrawArgs& a, const int2
 
 // Writes the drawn token and (p(y), q(y)) (thread 0).
 template <int DT>
-__device__ void finish_draw(const Params& P, const DrawArgs& a, double Sp, double Sq, int y,
+__device__ void finish_draw(const Params& P, const DrawArgs& a, DF Sp, DF Sq, int y,
                             int bonus_row) {
   float qy;
   const float zp = mask_below<DT>(Elem<DT & 1>::scalar(a.trow, y), a.tau_p);
-  const float py = (float)((double)exp2f(fmaf(zp, P.c, -a.mcp)) / Sp);
+  const float py = __fdiv_rn(exp2f(fmaf(zp, P.c, -a.mcp)), Sp.hi);
   if (a.kind == kResidual) {
     const float zq = mask_below<DT>(Elem<DT & 1>::scalar(a.drow, y), a.tau_q);
-    qy = (float)((double)exp2f(fmaf(zq, P.c, -a.mcq)) / Sq);
+    qy = __fdiv_rn(exp2f(fmaf(zq, P.c, -a.mcq)), Sq.hi);
   } else if (a.kind == kOneHot) {
     qy = (y == a.xhat) ? 1.f : 0.f;
   } else {
@@ -1091,7 +1084,7 @@ __device__ __noinline__ bool draw_part(const Params& P, Smem& s, unsigned char* 
   constexpr int TILE = kThreads * Elem<DT & 1>::kEPV;
   const int tid = threadIdx.x;
   const DrawDesc* d = &P.descs[slot];
-  const double Sp = __ldcg(&d->Sp), Sq = __ldcg(&d->Sq);
+  const DF Sp = ldcg_df(&d->Sp), Sq = ldcg_df(&d->Sq);
   const int kind = __ldcg(&d->kind);
   const DrawArgs a = make_draw_args(P, (size_t)P.V * Elem<DT & 1>::kBytes, __ldcg(&d->row),
                                     __ldcg(&d->drow), kind, __ldcg(&d->xhat), __ldcg(&d->mcp),
@@ -1104,12 +1097,12 @@ __device__ __noinline__ bool draw_part(const Params& P, Smem& s, unsigned char* 
   const int tile0 = part * cpp * kVPT;
   const int tile1 = min(ntiles, (part + 1) * cpp * kVPT);
   const int ntl = tile1 - tile0;
-  double* tsum = P.tsum + (size_t)slot * P.tsum_stride;
+  DF* tsum = P.tsum + (size_t)slot * P.tsum_stride;
   if (ntl > 0) {
     if (!tile_sums<DT, VEC>(P, s, ring, a, tile0, ntl)) return false;
     if (tid < ntl) {
-      double tt = 0.0;
-      for (int w = 0; w < kWarps; ++w) tt += (double)s.wtot[tid * kWarps + w];
+      DF tt{0.f, 0.f};
+      for (int w = 0; w < kWarps; ++w) tt = df_add_f(tt, s.wtot[tid * kWarps + w]);
       tsum[tile0 + tid] = tt;
     }
   }
@@ -1123,7 +1116,7 @@ __device__ __noinline__ bool draw_part(const Params& P, Smem& s, unsigned char* 
   if (!s.last) return true;
   // Last part: every tile sum is in the workspace.
   __threadfence();
-  const double tt = tid < ntiles ? __ldcg(&tsum[tid]) : 0.0;
+  const DF tt = tid < ntiles ? ldcg_df(&tsum[tid]) : DF{0.f, 0.f};
   int y = locate_token<DT, VEC>(P, s, a, tt, ntiles);
   DrawArgs used = a;
   if (y < 0 && kind != kBonus) {
@@ -1177,7 +1170,7 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
       kind = kOneHot;
     }
   }
-  const double Sp = __ldcg(&P.rows[srow].S_p), Sq = __ldcg(&P.rows[srow].S_q);
+  const DF Sp = ldcg_df(&P.rows[srow].S_p), Sq = ldcg_df(&P.rows[srow].S_q);
   const float mcp = __ldcg(&P.rows[srow].mc_p), mcq = __ldcg(&P.rows[srow].mc_q);
   if constexpr (VEC && (DT & kFilt) != 0) {
     // A filtered stop row with its kept logits listed: the draw reads the
@@ -1213,7 +1206,7 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
                                       mcp, mcq, Sp, Sq);
     constexpr int TILE = kThreads * Elem<DT & 1>::kEPV;
     const int ntiles = (P.V + TILE - 1) / TILE;
-    const double tt = tid < ntiles ? __ldcg(&P.btile[(size_t)b * P.tsum_stride + tid]) : 0.0;
+    const DF tt = tid < ntiles ? ldcg_df(&P.btile[(size_t)b * P.tsum_stride + tid]) : DF{0.f, 0.f};
     int y = locate_token<DT, VEC>(P, s, a, tt, ntiles);
     if (y < 0) {
       if (tid == 0) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
@@ -1314,38 +1307,16 @@ __device__ __forceinline__ int stop_from_state(unsigned long long st, int K) {
   return ((st >> K) & 1ull) ? K : -1;           // all accepted: needs the bonus row
 }
 
-// Row metadata of target row t into shared memory (thread 0).
-// Largest b in [0, B) with cu[b] <= j (the request owning draft slot j), by
-// a whole warp as find_request_warp.
-__device__ __forceinline__ int find_draft_request_warp(const int32_t* cu, int B, int j, int lane) {
-  int lo = 0, n = B;
-  while (n > 1) {
-    const int step = (n + 31) >> 5;
-    const int c = lo + lane * step;
-    const bool pass = c < lo + n && cu[c] <= j;
-    const unsigned m = __ballot_sync(kFull, pass);
-    const int k = 31 - __clz(m);
-    const int end = lo + n;
-    lo += k * step;
-    n = min(step, end - lo);
-  }
-  return lo;
-}
-
-// Run by warp 0: the row at position o of the work order.
-__device__ __noinline__ void row_meta(const Params& P, Smem& s, int o) {
+// Run by warp 0: the row at position o of the work order, of request b.
+__device__ __noinline__ void row_meta(const Params& P, Smem& s, int o, int b) {
   const int lane = threadIdx.x & 31;
-  int b, t;
-  if (!kBonusLast) {
+  int t;
+  if (!kBonusLast)
     t = o;
-    b = find_request_warp(P.cu, P.B, t, lane);
-  } else if (o < s.R_d) {  // draft-slot rows first, in order
-    b = find_draft_request_warp(P.cu, P.B, o, lane);
+  else if (o < s.R_d)  // draft-slot rows first, in order
     t = o + b;
-  } else {                 // then the bonus rows
-    b = o - s.R_d;
+  else                 // then the bonus rows
     t = P.cu[b + 1] + b;
-  }
   // The accept uniform is needed only after the row pass: load it now.
   const float u = (lane == 0 && P.uniforms) ? __ldg(&P.uniforms[2 * (size_t)t]) : 0.f;
   if (lane != 0) return;
@@ -1439,7 +1410,7 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
       warp_argmax(v, ix);
       if (lane == 0) {
         st.mc_p = st.mc_q = 0.f;
-        st.S_p = st.S_q = 0.0;
+        st.S_p = st.S_q = DF{0.f, 0.f};
         st.amax_v = v;
         st.amax_i = ix;
       }
@@ -1510,12 +1481,12 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
         stats_pass_scalar<DT, false>(trow, drow, V, P.c, at, ad, s.tau_t, s.tau_d);
     }
     float mcp, mcq;
-    double Sp, Sq;
+    DF Sp, Sq;
     combine_softmax<EPV>(at, ad, has_d, P.c, s, mcp, Sp, mcq, Sq);
     if (VEC && btiles && ok) {
       // Tile sums of r = 2^(z c - mc_p) over this slice's tiles: each warp's
       // part rescaled from its chunk offset to the slice's, summed over the
-      // warps in fp64. (A split row's merge rescales them to the row's.)
+      // warps in double-float. (A split row's merge rescales them to the row's.)
       if (tid == 0) s.bcast_f[0] = mcp;
       __syncthreads();
       const float M = s.bcast_f[0];
@@ -1525,11 +1496,11 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
       const int l = c0 * kVPT + tid;
       if (tid < (c1 - c0) * kVPT && l < ntiles) {
         const int k = tid / kVPT;
-        double T = 0.0;
+        DF T{0.f, 0.f};
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
           const float r = bref[k * kWarps + w];
-          if (r > -INFINITY) T += (double)(s.wtot[l * kWarps + w] * ex2(r - M));
+          if (r > -INFINITY) T = df_add_f(T, s.wtot[l * kWarps + w] * ex2(r - M));
         }
         P.btile[(size_t)b * P.tsum_stride + l] = T;
         __threadfence();  // visible to a split row's merging CTA before this part counts as done
@@ -1553,29 +1524,26 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
 // the calling warp; the result is valid in lane 0. The offset is the largest
 // exponent offset of the parts with mass, each part's sum is rescaled to it
 // by 2^(mc_r - mc) (the fp32 exponential the whole-row combine also uses) and
-// summed in fp64; greedy rows take the largest logit, lowest index on ties.
+// summed in double-float; greedy rows take the largest logit, lowest index on ties.
 __device__ __noinline__ PartRec merge_parts(const PartRec* parts, int n) {
   const int lane = threadIdx.x & 31;
   float mp = 0.f, mq = 0.f, av = -INFINITY;
-  double sp = 0.0, sq = 0.0;
+  DF sp{0.f, 0.f}, sq{0.f, 0.f};
   int ai = 0x7fffffff;
   if (lane < n) {
     mp = __ldcg(&parts[lane].mc_p);
     mq = __ldcg(&parts[lane].mc_q);
-    sp = __ldcg(&parts[lane].S_p);
-    sq = __ldcg(&parts[lane].S_q);
+    sp = ldcg_df(&parts[lane].S_p);
+    sq = ldcg_df(&parts[lane].S_q);
     av = __ldcg(&parts[lane].amax_v);
     ai = __ldcg(&parts[lane].amax_i);
   }
-  const bool hp = sp > 0.0, hq = sq > 0.0;
+  const bool hp = df_pos(sp), hq = df_pos(sq);
   const float Mp = warp_max(hp ? mp : -INFINITY), Mq = warp_max(hq ? mq : -INFINITY);
-  double wp = hp ? sp * (double)ex2(mp - Mp) : 0.0;
-  double wq = hq ? sq * (double)ex2(mq - Mq) : 0.0;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    wp += __shfl_xor_sync(kFull, wp, o);
-    wq += __shfl_xor_sync(kFull, wq, o);
-  }
+  DF wp = hp ? df_mul_f(sp, ex2(mp - Mp)) : DF{0.f, 0.f};
+  DF wq = hq ? df_mul_f(sq, ex2(mq - Mq)) : DF{0.f, 0.f};
+  wp = warp_sum_df(wp);
+  wq = warp_sum_df(wq);
   warp_argmax(av, ai);
   PartRec m;
   m.mc_p = Mp == -INFINITY ? 0.f : Mp;
@@ -1599,7 +1567,7 @@ __device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const P
   if (greedy) {
     const int am = (st.amax_i == 0x7fffffff) ? 0 : st.amax_i;  // all -inf: index 0, like argmax
     rec.mc_p = rec.mc_q = 0.f;
-    rec.S_p = rec.S_q = 0.0;
+    rec.S_p = rec.S_q = DF{0.f, 0.f};
     rec.argmax = am;
     rec.accept = (i < K && xhat == am) ? 1u : 0u;
     if (P.out_probs && i < K) {
@@ -1608,14 +1576,14 @@ __device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const P
     }
   } else {
     const float mcp = st.mc_p, mcq = st.mc_q;
-    const double Sp = st.S_p, Sq = st.S_q;
+    const DF Sp = st.S_p, Sq = st.S_q;
     rec.mc_p = mcp;
     rec.mc_q = mcq;
     rec.S_p = Sp;
     rec.S_q = Sq;
     rec.argmax = 0;
     rec.accept = (i == K && s.btile_ok) ? 3u : 1u;
-    if (!(Sp > 0.0) || (has_d && !(Sq > 0.0))) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
+    if (!df_pos(Sp) || (has_d && !df_pos(Sq))) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
     if (i < K) {
       float ph = -1.f, qh = -1.f;
       unsigned acc = 0u;
@@ -1628,7 +1596,7 @@ __device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const P
         // most), far inside the 1e-6 within which a decision counts as a tie
         // with the float64 evaluation; fp64 divisions cost this step more on
         // this part than the bytes it saves.
-        const float Spf = (float)Sp, Sqf = (float)Sq;
+        const float Spf = Sp.hi, Sqf = Sq.hi;
         const float pd = __fdiv_rn(exp2f(ap), Spf);
         float rho, qd = 1.f;
         if (has_d) {
@@ -1689,7 +1657,10 @@ template <int DT, bool VEC>
 __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int o, int part,
                              int split) {
   const int tid = threadIdx.x;
-  if (tid < 32) row_meta(P, s, o);
+  // The row's request: the whole CTA searches the offsets.
+  const int bq = !kBonusLast ? find_request_cta(P.cu, P.B, o, true)
+                 : (o < s.R_d ? find_request_cta(P.cu, P.B, o, false) : o - s.R_d);
+  if (tid < 32) row_meta(P, s, o, bq);
   __syncthreads();
   const int b = s.b, t = s.t, t0 = s.t0, d0 = s.d0, K = s.K, i = s.i;
   const bool greedy = s.greedy != 0;
@@ -1721,9 +1692,9 @@ __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int 
         int ok = !greedy && ft.ok && fd.ok;
         if (ok) {
           st.mc_p = ft.mc;
-          st.S_p = ft.S;
+          st.S_p = df_from_d(ft.S);
           st.mc_q = has_d ? fd.mc : 0.f;
-          st.S_q = has_d ? fd.S : 0.0;
+          st.S_q = has_d ? df_from_d(fd.S) : DF{0.f, 0.f};
           st.amax_v = -INFINITY;
           st.amax_i = 0x7fffffff;
           const int xh = s.xhat;
@@ -1770,10 +1741,10 @@ __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int 
       const int cpp = (nch + np - 1) / np;
       for (int l = tid; l < ntiles; l += kThreads) {
         const PartRec* pr = P.parts + (size_t)split * np + (l / kVPT) / cpp;
-        const double Sp_part = __ldcg(&pr->S_p);
-        const float f = Sp_part > 0.0 ? ex2(__ldcg(&pr->mc_p) - M) : 0.f;
-        double* bt = P.btile + (size_t)b * P.tsum_stride + l;
-        *bt = __ldcg(bt) * (double)f;
+        const DF Sp_part = ldcg_df(&pr->S_p);
+        const float f = df_pos(Sp_part) ? ex2(__ldcg(&pr->mc_p) - M) : 0.f;
+        DF* bt = P.btile + (size_t)b * P.tsum_stride + l;
+        *bt = df_mul_f(ldcg_df(bt), f);
       }
       if (tid == 0) s.btile_ok = 1;
     }
@@ -1928,8 +1899,8 @@ static WsLayout ws_layout(long long B, int V) {
   L.slot_state = L.req_done + align16((size_t)B * sizeof(unsigned long long));
   L.descs = L.slot_state + align16(S * sizeof(unsigned));
   L.tsum = L.descs + S * sizeof(DrawDesc);
-  L.btile = L.tsum + align16(S * (size_t)tsum_stride(V) * sizeof(double));
-  L.part_done = L.btile + align16((size_t)B * tsum_stride(V) * sizeof(double));
+  L.btile = L.tsum + align16(S * (size_t)tsum_stride(V) * sizeof(DF));
+  L.part_done = L.btile + align16((size_t)B * tsum_stride(V) * sizeof(DF));
   L.parts = L.part_done + align16((size_t)kMaxTailRows * sizeof(unsigned));
   L.rows = L.parts + (size_t)kMaxPartRecs * sizeof(PartRec);
   return L;
@@ -2044,8 +2015,8 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
   P.req_state = reinterpret_cast<unsigned long long*>(ws + L.req_done);
   P.slot_state = reinterpret_cast<unsigned*>(ws + L.slot_state);
   P.descs = reinterpret_cast<DrawDesc*>(ws + L.descs);
-  P.tsum = reinterpret_cast<double*>(ws + L.tsum);
-  P.btile = reinterpret_cast<double*>(ws + L.btile);
+  P.tsum = reinterpret_cast<DF*>(ws + L.tsum);
+  P.btile = reinterpret_cast<DF*>(ws + L.btile);
   P.n_slots = n_draw_slots(B);
   P.part_done = reinterpret_cast<unsigned*>(ws + L.part_done);
   P.parts = reinterpret_cast<PartRec*>(ws + L.parts);

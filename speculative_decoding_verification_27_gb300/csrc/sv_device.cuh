@@ -261,7 +261,7 @@ __device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
 
 // Double-float value hi + lo (|lo| <= ulp(hi)/2): error-free transformations
 // keep sums of fp32 partials accurate to ~2^-44 relative without fp64 math.
-struct DF {
+struct alignas(8) DF {
   float hi, lo;
 };
 
@@ -309,6 +309,15 @@ __device__ __forceinline__ DF df_div(DF a, DF b) {
 }
 
 __device__ __forceinline__ double df_to_d(DF a) { return (double)a.hi + (double)a.lo; }
+__device__ __forceinline__ DF df_from_d(double d) {
+  const float hi = (float)d;
+  return {hi, (float)(d - (double)hi)};
+}
+// An 8-byte global load that bypasses L1 (data another CTA may have written).
+__device__ __forceinline__ DF ldcg_df(const DF* p) {
+  const float2 v = __ldcg(reinterpret_cast<const float2*>(p));
+  return {v.x, v.y};
+}
 
 // ---------------------------------------------------------------------------
 // Warp / CTA reductions (kThreads threads, all participating)
