@@ -90,9 +90,10 @@ enum { SV_MODE_SAMPLE = 0, SV_MODE_GREEDY = 1 };
 /*
  * Bytes of workspace spec_verify / spec_verify_greedy need for B requests,
  * R_t target rows and vocabulary size V (0 if an argument is out of range).
- * The workspace holds a 64-byte header, an 8-byte progress word per request, a 32-byte
- * record per target row, the tile sums (8 bytes per 1024 vocabulary entries)
- * that each request's bonus row leaves for its draw, a fixed 528 KiB region
+ * The workspace holds a 64-byte header, an 8-byte progress word per request,
+ * per target row a 32-byte record and the tile sums (4 bytes per 1024
+ * vocabulary entries) that a row streamed alone (a bonus row, or a draft
+ * slot with a one-hot proposal) leaves for a draw there, a fixed 528 KiB region
  * for rows that the kernel splits across CTAs near the end of a call, and,
  * for up to min(B, 4096) final draws it splits the same way, a descriptor and
  * the partial sums of each. It must be 16-byte aligned and zero-filled
@@ -171,9 +172,9 @@ sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype, int32_t 
  *     few rows, where the persistent kernel's time is a chain of dependent
  *     steps rather than bytes.
  * The cluster kernel runs when the workspace holds at most `rows` target
- * rows ((workspace_bytes - spec_verify_workspace_size(B, 0, V)) / 32 <=
- * rows; a workspace sized for R_t holds R_t), the rows are 16-byte aligned
- * with V * element size a multiple of 16, and a row pair fits 200 KB of
+ * rows (a workspace of spec_verify_workspace_size(B, R_t, V) bytes holds
+ * R_t; each further row takes 32 + 4 * ceil(V / 1024) bytes), the rows are
+ * 16-byte aligned with V * element size a multiple of 16, and a row pair fits 200 KB of
  * shared memory per CTA (V * element size <= 800 KB with draft rows, 1.6 MB
  * without). The filtered and no-allocation entry points always take the
  * persistent kernel.
@@ -252,8 +253,10 @@ sv_status spec_verify_filtered(const void* target_logits, const void* draft_logi
  * or by the caller.
  *
  * Limit. The fixed block holds SV_NOALLOC_SCRATCH_BYTES (4 MiB). A batch
- * fits when spec_verify_workspace_size(B, R_t, V) <= SV_NOALLOC_SCRATCH_BYTES
- * (for example B = 256, K = 7, V = 151936 needs about 0.9 MiB).
+ * fits when spec_verify_workspace_size(B, 0, V) + 32 * R_t <=
+ * SV_NOALLOC_SCRATCH_BYTES (for example B = 256, K = 7, V = 151936 needs
+ * about 0.9 MiB): the block keeps a 32-byte record per row and no per-row
+ * tile sums, so a draw at a bonus or one-hot row reads its row again.
  *   - If B and V alone need more than the block, the call returns
  *     SV_ERR_INVALID_ARG before anything is enqueued.
  *   - R_t is known only on the device (cu_draft[B] + B). If the rows do not

@@ -67,8 +67,10 @@ struct alignas(16) RowRec {
   DF S_p;            // sum_x 2^(z_x c - mc_p) over the target row (double-float)
   DF S_q;            // same over the draft row
   int argmax;        // greedy rows: first index of the maximum
-  unsigned accept;   // bit 0: the slot's draft token is accepted; bit 1 (bonus
-                     // rows): the tile sums of r = 2^(z c - mc_p) are stored
+  unsigned accept;   // bit 0: the slot's draft token is accepted; bit 1: the
+                     // row's tile sums of its draw's r are stored (rows streamed
+                     // alone: bonus rows r = 2^(z c - mc_p), one-hot rows the same
+                     // without x̂)
 };
 static_assert(sizeof(RowRec) == 32, "row record is 32 bytes");
 
@@ -192,7 +194,7 @@ struct Params {
   unsigned int* slot_state; // [n_slots] nparts << 20 | parts handed out (0: unpublished)
   DrawDesc* descs;          // [n_slots]
   DF* tsum;                 // [n_slots, tsum_stride] per-tile sums of r
-  DF* btile;                // [B, tsum_stride] tile sums of a bonus row's r = S_p p
+  float* rtile;             // [row_cap, tsum_stride] tile sums of r of rows streamed alone, or NULL
   const float* thr;         // [R_t] filter thresholds of the target rows, or NULL
   const float* thr_d;       // [R_d] filter thresholds of the draft rows, or NULL
   const FStat* fst;         // [R_t] filtered softmax statistics of the target rows, or NULL
@@ -216,7 +218,7 @@ struct Smem {
   int b, t, t0, d0, K, i, greedy, xhat, last, stop, merge, pick, pick2, tok, R_d;
   int zx_ok;        // z_p(x̂) (and z_q(x̂)) were taken from the ring during the row pass
   int pre;          // filtered row: its statistics came from the threshold kernel
-  int btile_ok;     // this bonus row's tile sums were stored during its pass
+  int btile_ok;     // this row's tile sums of r were stored during its pass
   float tau_t, tau_d;  // filter thresholds of the row pair (-inf: unfiltered)
   float zx_p, zx_q, u_acc;
   float redf[kWarps];
@@ -1143,8 +1145,7 @@ template <int DT, bool VEC>
 __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned char* ring, int b,
                                             int t0, int d0, int K, bool greedy) {
   const int tid = threadIdx.x;
-  const int stop = s.stop;  // set by the row that decided it
-  if (tid == 0) __threadfence();
+  const int stop = s.stop;  // set by the row that decided it (its update acquired the rows' records)
   for (int j = tid; j < stop; j += kThreads) P.out_tokens[t0 + j] = P.draft_tokens[d0 + j];
   const int srow = t0 + stop;
   if (tid == 0) P.out_len[b] = stop + 1;
@@ -1199,15 +1200,46 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
       return true;
     }
   }
-  if (VEC && kind == kBonus && (__ldcg(&P.rows[srow].accept) & 2u)) {
-    // The bonus row left its tile sums: only the chosen tile is read again.
+  if (VEC && (kind == kBonus || kind == kOneHot) && (__ldcg(&P.rows[srow].accept) & 2u)) {
+    // The stop row left the tile sums of r (a bonus row: p; a one-hot row:
+    // p without x̂): only the chosen tile is read again.
     if (tid == 0) atomicAdd(&P.ws->committed, 1u);
     const DrawArgs a = make_draw_args(P, (size_t)P.V * Elem<DT & 1>::kBytes, srow, drow, kind, xhat,
                                       mcp, mcq, Sp, Sq);
-    constexpr int TILE = kThreads * Elem<DT & 1>::kEPV;
+    constexpr int EPV = Elem<DT & 1>::kEPV;
+    constexpr int TILE = kThreads * EPV;
     const int ntiles = (P.V + TILE - 1) / TILE;
-    const DF tt = tid < ntiles ? ldcg_df(&P.btile[(size_t)b * P.tsum_stride + tid]) : DF{0.f, 0.f};
+    DF tt{tid < ntiles ? __ldcg(&P.rtile[(size_t)srow * P.tsum_stride + tid]) : 0.f, 0.f};
+    if (kind == kOneHot && xhat >= 0) {
+      // The row's tiles hold every term of p; x̂'s tile is summed again
+      // without x̂ (afresh, so a dominant x̂ leaves no rounding behind).
+      const int lx = xhat / TILE;
+      float z[EPV], r[EPV];
+      load_chunk<DT & 1, VEC>(a.trow, lx * TILE + tid * EPV, P.V, z);
+      mask_below<DT>(z, a.tau_p);
+      residual_of<EPV>(a, P.c, z, z, lx * TILE + tid * EPV, r);
+      float m = 0.f;
+#pragma unroll
+      for (int j = 0; j < EPV; ++j) m += r[j];
+      const DF w = warp_sum_df(DF{m, 0.f});
+      if ((tid & 31) == 0) s.reddf_p[tid >> 5] = w;
+      __syncthreads();
+      if (tid == lx) {
+        DF sum = s.reddf_p[0];
+        for (int k = 1; k < kWarps; ++k) sum = df_add(sum, s.reddf_p[k]);
+        tt = sum;
+      }
+      __syncthreads();
+    }
     int y = locate_token<DT, VEC>(P, s, a, tt, ntiles);
+    if (y < 0 && kind == kOneHot) {
+      // No mass besides x̂: draw from p instead.
+      if (tid == 0) atomicOr(&P.ws->status, SV_DATA_DEGENERATE_RESIDUAL);
+      DrawArgs used = a;
+      used.kind = kBonus;
+      y = draw_whole<DT, VEC>(P, s, ring, used);
+      if (y == -2) return false;
+    }
     if (y < 0) {
       if (tid == 0) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
       y = 0;
@@ -1360,7 +1392,7 @@ __device__ __noinline__ void row_meta(const Params& P, Smem& s, int o, int b) {
 template <int DT, bool VEC>
 __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const char* trow,
                             const char* drow, bool greedy, int c0, int c1, PartRec& st,
-                            bool btiles, int b) {
+                            bool btiles, int t) {
   constexpr int EPV = Elem<DT & 1>::kEPV;
   constexpr int CH = kChunkBytes / Elem<DT & 1>::kBytes;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1433,14 +1465,15 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
         jx = (e - kx * CH) % EPV;
         if (vi % kThreads != tid) kx = -1;
       }
-      // A bonus row (whole, r = S_p p if it is drawn from) also leaves, per
-      // tile and warp, the sum of its terms relative to a per-chunk warp
-      // offset, in the draw's scratch (idle during a row pass).
+      // A row streamed alone (a bonus row, or a one-hot draft slot) also
+      // leaves, per tile and warp, the sum of its draw's terms relative to a
+      // per-chunk warp offset, in the draw's scratch (idle during a row pass):
+      // r = 2^(z c - mc), without x̂ for a one-hot slot, so that a draw at
+      // this row reads none of it again.
       float* bref = reinterpret_cast<float*>(s.tincl);  // [chunk][warp] offsets
       constexpr int TILE = kThreads * EPV;
       const int ntiles = (V + TILE - 1) / TILE;
       if (btiles) {
-        // Bonus rows stream alone (no draft row, no proposed token).
         ok = ring_stream(s, ring, trow + off, nullptr, len, false, [&](int k, uint32_t stage) {
           uint4 rv[kVPT];
           stage_vectors<DT>(stage, x0 + k * CH, V, rv, s.tau_t);
@@ -1502,7 +1535,7 @@ __device__ bool slice_stats(const Params& P, Smem& s, unsigned char* ring, const
           const float r = bref[k * kWarps + w];
           if (r > -INFINITY) T = df_add_f(T, s.wtot[l * kWarps + w] * ex2(r - M));
         }
-        P.btile[(size_t)b * P.tsum_stride + l] = T;
+        P.rtile[(size_t)t * P.tsum_stride + l] = T.hi + T.lo;
         __threadfence();  // visible to a split row's merging CTA before this part counts as done
       }
       if (tid == 0) s.btile_ok = 1;
@@ -1582,7 +1615,7 @@ __device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const P
     rec.S_p = Sp;
     rec.S_q = Sq;
     rec.argmax = 0;
-    rec.accept = (i == K && s.btile_ok) ? 3u : 1u;
+    rec.accept = (i == K && s.btile_ok) ? 3u : 1u;  // bonus rows count as accepted
     if (!df_pos(Sp) || (has_d && !df_pos(Sq))) atomicOr(&P.ws->status, SV_DATA_EMPTY_ROW);
     if (i < K) {
       float ph = -1.f, qh = -1.f;
@@ -1611,7 +1644,7 @@ __device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const P
         ph = pd;
         qh = qd;
       }
-      rec.accept = acc;
+      rec.accept = acc | (s.btile_ok ? 2u : 0u);
       if (P.out_probs) {
         P.out_probs[2 * (size_t)t] = ph;
         P.out_probs[2 * (size_t)t + 1] = qh;
@@ -1619,13 +1652,13 @@ __device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const P
     }
   }
   P.rows[t] = rec;
-  __threadfence();
   // s.last: this row makes the request's stop slot known (commit here);
-  // s.stop: that slot.
+  // s.stop: that slot. The progress update releases this row's record and
+  // acquires those of the rows counted before it (read by the commit).
   s.last = 0;
   if (K <= kMaxTrackedK) {
-    const unsigned long long add = (1ull << i) | (rec.accept && i < K ? 1ull << (32 + i) : 0ull);
-    const unsigned long long old = atomicOr(&P.req_state[b], add);
+    const unsigned long long add = (1ull << i) | ((rec.accept & 1u) && i < K ? 1ull << (32 + i) : 0ull);
+    const unsigned long long old = atom_or_acqrel_gpu(&P.req_state[b], add);
     const unsigned long long now = old | add;
     const int stop = stop_from_state(now, K);
     if (stop >= 0 && stop_from_state(old, K) < 0) {
@@ -1635,12 +1668,11 @@ __device__ __noinline__ void decide_row(const Params& P, Smem& s, int t, const P
     const unsigned long long all = (K + 1 == 64) ? ~0ull : ((1ull << (K + 1)) - 1ull);
     if ((now & all) == all) P.req_state[b] = 0ull;  // every row is in: reset for the next call
   } else {
-    const unsigned long long old = atomicAdd(&P.req_state[b], 1ull);
+    const unsigned long long old = atom_add_acqrel_gpu(&P.req_state[b], 1ull);
     if (old == (unsigned long long)K) {
-      __threadfence();
       int stop = K;
       for (int j = 0; j < K; ++j)
-        if (__ldcg(&P.rows[t0_of(P, b) + j].accept) == 0u) {
+        if ((__ldcg(&P.rows[t0_of(P, b) + j].accept) & 1u) == 0u) {
           stop = j;
           break;
         }
@@ -1677,7 +1709,9 @@ __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int 
     c1 = min(nch, c0 + cpp);
   }
   PartRec st;
-  const bool btiles = VEC && i == K && !greedy;
+  // Rows streamed alone keep their draw's tile sums: bonus rows, and draft
+  // slots with one-hot proposals (no draft row).
+  const bool btiles = VEC && P.rtile != nullptr && !greedy && (i == K || !has_d);
   bool pre = false;
   if constexpr ((DT & kFilt) != 0) {
     // A whole filtered row whose threshold kernel left its statistics (and
@@ -1710,17 +1744,13 @@ __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int 
       pre = s.pre != 0;
     }
   }
-  if (!pre && !slice_stats<DT, VEC>(P, s, ring, trow, drow, greedy, c0, c1, st, btiles, b)) return false;
+  if (!pre && !slice_stats<DT, VEC>(P, s, ring, trow, drow, greedy, c0, c1, st, btiles, t)) return false;
   if (part >= 0) {
     if (tid == 0) {
       P.parts[(size_t)split * np + part] = st;
-      __threadfence();
-      const unsigned old = atomicAdd(&P.part_done[split], 1u);
+      const unsigned old = atom_add_acqrel_gpu(&P.part_done[split], 1u);
       s.merge = (old == (unsigned)np - 1u) ? 1 : 0;  // this CTA merges the row
-      if (s.merge) {
-        __threadfence();
-        P.part_done[split] = 0u;
-      }
+      if (s.merge) P.part_done[split] = 0u;
     }
     __syncthreads();
     if (!s.merge) return true;
@@ -1743,8 +1773,8 @@ __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int 
         const PartRec* pr = P.parts + (size_t)split * np + (l / kVPT) / cpp;
         const DF Sp_part = ldcg_df(&pr->S_p);
         const float f = df_pos(Sp_part) ? ex2(__ldcg(&pr->mc_p) - M) : 0.f;
-        DF* bt = P.btile + (size_t)b * P.tsum_stride + l;
-        *bt = df_mul_f(ldcg_df(bt), f);
+        float* bt = P.rtile + (size_t)t * P.tsum_stride + l;
+        *bt = __ldcg(bt) * f;
       }
       if (tid == 0) s.btile_ok = 1;
     }
@@ -1854,10 +1884,8 @@ __global__ void __launch_bounds__(kThreads, SV_MINBLOCKS) verify_kernel(Params P
   }
   // The last CTA to leave clears the draw slots and the counters.
   if (tid == 0) {
-    __threadfence();
-    const unsigned old = atomicAdd(&P.ws->exited, 1u);
+    const unsigned old = atom_add_acqrel_gpu(&P.ws->exited, 1u);
     s.last = (old == gridDim.x - 1) ? 1 : 0;
-    if (s.last) __threadfence();
   }
   __syncthreads();
   if (!s.last) return;
@@ -1887,9 +1915,9 @@ static int n_draw_slots(long long B) { return (int)(B < kMaxDrawSlots ? B : kMax
 static int tsum_stride(int V) { return (V + kThreads * 4 - 1) / (kThreads * 4); }
 
 // header | req_state[B] | slot_state[S] | descs[S] | tsum[S][stride] |
-// btile[B][stride] | part_done[kMaxTailRows] | parts[kMaxPartRecs] | rows[R_t]
+// part_done[kMaxTailRows] | parts[kMaxPartRecs] | rows[R_t] | rtile[R_t][stride]
 struct WsLayout {
-  size_t req_done, slot_state, descs, tsum, btile, part_done, parts, rows;
+  size_t req_done, slot_state, descs, tsum, part_done, parts, rows;
 };
 
 static WsLayout ws_layout(long long B, int V) {
@@ -1899,15 +1927,17 @@ static WsLayout ws_layout(long long B, int V) {
   L.slot_state = L.req_done + align16((size_t)B * sizeof(unsigned long long));
   L.descs = L.slot_state + align16(S * sizeof(unsigned));
   L.tsum = L.descs + S * sizeof(DrawDesc);
-  L.btile = L.tsum + align16(S * (size_t)tsum_stride(V) * sizeof(DF));
-  L.part_done = L.btile + align16((size_t)B * tsum_stride(V) * sizeof(DF));
+  L.part_done = L.tsum + align16(S * (size_t)tsum_stride(V) * sizeof(DF));
   L.parts = L.part_done + align16((size_t)kMaxTailRows * sizeof(unsigned));
   L.rows = L.parts + (size_t)kMaxPartRecs * sizeof(PartRec);
   return L;
 }
 
+// Bytes per target row: its record and its tile sums.
+static size_t row_bytes(int V) { return sizeof(RowRec) + (size_t)tsum_stride(V) * sizeof(float); }
+
 static size_t ws_size(long long B, long long R_t, int V) {
-  return ws_layout(B, V).rows + (size_t)R_t * sizeof(RowRec);
+  return ws_layout(B, V).rows + (size_t)R_t * row_bytes(V);
 }
 
 // Resident CTAs per device for each kernel variant, filled on first use
@@ -1988,7 +2018,8 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
                             void* workspace, size_t workspace_bytes, void* stream,
                             int greedy_all, const float* thr = nullptr,
                             const float* thr_d = nullptr, const FStat* fst = nullptr,
-                            const FStat* fst_d = nullptr, const int2* flist = nullptr) {
+                            const FStat* fst_d = nullptr, const int2* flist = nullptr,
+                            int row_tiles = 1) {
   const sv_status chk = check_verify_args(target, draft, dtype, V, B, draft_tokens, cu_draft, uniforms,
                                           temperature, out_tokens, out_len, out_probs, greedy_all);
   if (chk != SV_OK || B == 0) return chk;
@@ -2016,13 +2047,16 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
   P.slot_state = reinterpret_cast<unsigned*>(ws + L.slot_state);
   P.descs = reinterpret_cast<DrawDesc*>(ws + L.descs);
   P.tsum = reinterpret_cast<DF*>(ws + L.tsum);
-  P.btile = reinterpret_cast<DF*>(ws + L.btile);
+
   P.n_slots = n_draw_slots(B);
   P.part_done = reinterpret_cast<unsigned*>(ws + L.part_done);
   P.parts = reinterpret_cast<PartRec*>(ws + L.parts);
   P.tsum_stride = tsum_stride(V);
   P.rows = reinterpret_cast<RowRec*>(ws + L.rows);
-  P.row_cap = (long long)((workspace_bytes - L.rows) / sizeof(RowRec));
+  // Rows and their tile sums share what follows the fixed part; without
+  // tiles (row_tiles == 0) the records alone fill it.
+  P.row_cap = (long long)((workspace_bytes - L.rows) / (row_tiles ? row_bytes(V) : sizeof(RowRec)));
+  P.rtile = row_tiles ? reinterpret_cast<float*>(ws + L.rows + (size_t)P.row_cap * sizeof(RowRec)) : nullptr;
   P.greedy_all = greedy_all;
   // Draws are published in parts only if they stream kMinPublishBytes or more.
   P.may_publish = !greedy_all && (size_t)V * es * (P.draft ? 2 : 1) >= kMinPublishBytes;
@@ -2126,7 +2160,8 @@ sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logit
   if (cudaMemsetAsync(scratch, 0, L.rows, st) != cudaSuccess) return SV_ERR_CUDA;
   const sv_status s = sv::run_verify(target_logits, draft_logits, dtype, V, B, draft_tokens,
                                      cu_draft, mode, uniforms, temperature, out_tokens, out_len,
-                                     out_probs, scratch, SV_NOALLOC_SCRATCH_BYTES, cuda_stream, 0);
+                                     out_probs, scratch, SV_NOALLOC_SCRATCH_BYTES, cuda_stream, 0,
+                                     nullptr, nullptr, nullptr, nullptr, nullptr, 0);
   if (s != SV_OK) return s;
   if (status_out && cudaMemcpyAsync(status_out, scratch, sizeof(uint32_t),
                                     cudaMemcpyDeviceToDevice, st) != cudaSuccess)

@@ -35,8 +35,8 @@ def test_workspace_size(lib):
         S = min(B, 4096)            # draw slots
         tiles = (V + 1023) // 1024  # tile sums per slot (fp32-sized tiles)
         split = a16(4 * 4096) + 32 * 16384  # counters and records of split rows
-        bonus = a16(8 * B * tiles)  # tile sums left by each request's bonus row
-        want = 64 + a16(8 * B) + a16(4 * S) + 64 * S + a16(8 * S * tiles) + bonus + split + 32 * R
+        per_row = 32 + 4 * tiles    # record + fp32 tile sums of a row streamed alone
+        want = 64 + a16(8 * B) + a16(4 * S) + 64 * S + a16(8 * S * tiles) + split + per_row * R
         assert api.spec_verify_workspace_size(B, R, V) == want
     assert lib.spec_verify_workspace_size(-1, 4, 10) == 0
     assert lib.spec_verify_workspace_size(4, 4, 0) == 0
