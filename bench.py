@@ -44,8 +44,8 @@ WORKLOAD = ("sampling verify B=256 K=7 V=151936 bf16 T=0.7, peaked rank-score ro
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per verify launch on this workload from one ncu
 # capture, valid only for the kernel sources whose hash is recorded with it.
-TRAFFIC = {"sources_sha256": "cef7f254000bddb4841b0f10ae9d59a5574c4671265a3f24be03cd1f20296402",
-           "bytes_per_launch": 1235726592 + 4355840,
+TRAFFIC = {"sources_sha256": "6e34605a287c386d0bdad4ef77835d52400b99f1b68302b33ecc465d15c24c9c",
+           "bytes_per_launch": 1235240704 + 5039616,
            "profile": "profiles/verify_kernel_sampling_B256_K7_V151936_bf16.md"}
 
 

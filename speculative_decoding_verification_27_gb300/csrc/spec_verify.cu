@@ -51,7 +51,7 @@ namespace sv {
 
 struct WsHeader {
   unsigned int status;     // SV_DATA_* bits (sticky until sv_check_status)
-  unsigned int next_item;  // next row to hand out
+  unsigned int next_item;  // items handed out by claims (every CTA's first item, blockIdx.x, is not claimed)
   unsigned int exited;     // CTAs that left the work loop
   unsigned int n_draws;    // draw slots reserved
   unsigned int draw_head;  // slots before this one are fully handed out
@@ -218,6 +218,7 @@ struct Smem {
   int b, t, t0, d0, K, i, greedy, xhat, last, stop, merge, pick, pick2, tok, R_d;
   int zx_ok;        // z_p(x̂) (and z_q(x̂)) were taken from the ring during the row pass
   int pre;          // filtered row: its statistics came from the threshold kernel
+  int claims;       // work items this CTA has asked for (thread 0)
   int btile_ok;     // this row's tile sums of r were stored during its pass
   float tau_t, tau_d;  // filter thresholds of the row pair (-inf: unfiltered)
   float zx_p, zx_q, u_acc;
@@ -1264,7 +1265,7 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
     const size_t draw_bytes = (size_t)P.V * Elem<DT & 1>::kBytes * (kind == kResidual ? 2 : 1);
     s.slot = -1;
     if (nparts > 1 && draw_bytes >= kMinPublishBytes &&
-        ld_relaxed_gpu(&P.ws->next_item) + kPublishPct * gridDim.x / 100u >= s.n_items) {
+        ld_relaxed_gpu(&P.ws->next_item) + gridDim.x + kPublishPct * gridDim.x / 100u >= s.n_items) {
       const unsigned slot = atomicAdd(&P.ws->n_draws, 1u);
       if (slot < (unsigned)P.n_slots) {
         DrawDesc* d = &P.descs[slot];
@@ -1808,6 +1809,7 @@ __global__ void __launch_bounds__(kThreads, SV_MINBLOCKS) verify_kernel(Params P
       fence_mbar_init();
     }
     s.ring_seq = 0;
+    s.claims = 0;
   }
   if (__syncthreads_or(bad)) {
     if (blockIdx.x == 0 && tid == 0) atomicOr(&P.ws->status, SV_DATA_BAD_OFFSETS);
@@ -1837,7 +1839,8 @@ __global__ void __launch_bounds__(kThreads, SV_MINBLOCKS) verify_kernel(Params P
     if (tid == 0) {
       // Rows first; once they are all handed out, parts of published draws.
       int slot = -1, part = -1;
-      const unsigned t = atomicAdd(&P.ws->next_item, 1u);
+      // A CTA's first item is its own index; later ones come from the counter.
+      const unsigned t = s.claims++ == 0 ? blockIdx.x : atomicAdd(&P.ws->next_item, 1u) + gridDim.x;
       s.wk = 0;
       if (t < n_items) {
         s.wk = 2;
