@@ -69,6 +69,24 @@ __device__ __forceinline__ void load_elems(const char* row, int x, int Vs, float
   load_chunk<DT, VEC>(row, x, Vs, f);
 }
 
+// Largest b in [0, B) with cu[b] + b <= t (the request owning target row t),
+// by every thread of the CTA at once: each round tests kT evenly spaced
+// candidates and one barrier counts the passing prefix (one round up to
+// B = kT).
+__device__ __forceinline__ int find_request_cta(const int32_t* cu, int B, int t) {
+  int lo = 0, n = B;
+  while (n > 1) {
+    const int step = (n + kT - 1) / kT;
+    const int c = lo + (int)threadIdx.x * step;
+    const bool pass = c < lo + n && cu[c] + c <= t;
+    const int cnt = __syncthreads_count(pass);
+    const int end = lo + n;
+    lo += (cnt - 1) * step;
+    n = min(step, end - lo);
+  }
+  return lo;
+}
+
 // Offsets of a packed ragged layout are valid for R_t target rows.
 __device__ __forceinline__ bool offsets_ok(const int32_t* cu, int B, long long R_t) {
   if (cu[0] != 0) return false;
@@ -95,7 +113,7 @@ template <int DT, bool VEC>
 __global__ void __launch_bounds__(kT) stats_kernel(StatParams P) {
   constexpr int EPV = Elem<DT>::kEPV;
   __shared__ float s_m[kW], s_zx;
-  __shared__ double s_S[kW];
+  __shared__ DF s_S[kW];
   __shared__ float s_av[kW];
   __shared__ int s_ai[kW], s_x, s_hx, s_ok;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -111,20 +129,17 @@ __global__ void __launch_bounds__(kT) stats_kernel(StatParams P) {
   __syncthreads();
   if (!s_ok) return;
   for (int r = blockIdx.x; r < P.rows; r += gridDim.x) {
+    // The row's proposed token: draft rows carry their own; target row
+    // (b, i) carries draft slot i's when i < K_b (none for the bonus row).
+    // The whole CTA finds the request of a target row.
+    const int rb = P.is_draft ? 0 : find_request_cta(P.cu, P.B, r);
     if (tid == 0) {
-      // The row's proposed token: draft rows carry their own; target row
-      // (b, i) carries draft slot i's when i < K_b (none for the bonus row).
       int x = -1;
       if (P.is_draft) {
         x = P.tokens[r];
       } else {
-        int lo = 0, hi = P.B - 1;  // largest b with cu[b] + b <= r
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (P.cu[mid] + mid <= r) lo = mid; else hi = mid - 1;
-        }
-        const int i = r - (P.cu[lo] + lo), K = P.cu[lo + 1] - P.cu[lo];
-        x = (i < K && P.tokens) ? P.tokens[P.cu[lo] + i] : -1;
+        const int i = r - (P.cu[rb] + rb), K = P.cu[rb + 1] - P.cu[rb];
+        x = (i < K && P.tokens) ? P.tokens[P.cu[rb] + i] : -1;
       }
       s_x = x;
       s_hx = 0;
@@ -135,9 +150,7 @@ __global__ void __launch_bounds__(kT) stats_kernel(StatParams P) {
     const char* row = P.logits + (long long)r * P.ld_bytes;
     float m = -INFINITY, mc = 0.f, sum = 0.f, av = -INFINITY;
     int ai = INT_MAX;
-    for (int e = tid * EPV; e < P.Vs; e += kT * EPV) {
-      float f[EPV];
-      load_elems<DT, VEC>(row, e, P.Vs, f);
+    auto fold = [&](const float (&f)[EPV], int e) {
       float vm = f[0];
 #pragma unroll
       for (int j = 1; j < EPV; ++j) vm = fmaxf(vm, f[j]);
@@ -159,6 +172,35 @@ __global__ void __launch_bounds__(kT) stats_kernel(StatParams P) {
           s_hx = 1;
         }
       }
+    };
+    if constexpr (VEC) {
+      // kU 16-byte loads in flight per thread before any is used.
+      constexpr int kU = 8;
+      for (int e0 = tid * EPV; e0 < P.Vs; e0 += kT * EPV * kU) {
+        uint4 raw[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int e = e0 + u * kT * EPV;
+          raw[u] = e < P.Vs ? ld_stream16(row + (size_t)e * Elem<DT>::kBytes)
+                            : (DT == 1 ? make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u)
+                                       : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u));
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int e = e0 + u * kT * EPV;
+          if (e < P.Vs) {
+            float f[EPV];
+            Elem<DT>::unpack(raw[u], f);
+            fold(f, e);
+          }
+        }
+      }
+    } else {
+      for (int e = tid * EPV; e < P.Vs; e += kT * EPV) {
+        float f[EPV];
+        load_elems<DT, VEC>(row, e, P.Vs, f);
+        fold(f, e);
+      }
     }
     // CTA combine: maximum, then every thread's sum rescaled to its offset.
     const float wm = warp_max(m);
@@ -173,19 +215,21 @@ __global__ void __launch_bounds__(kT) stats_kernel(StatParams P) {
 #pragma unroll
     for (int w = 1; w < kW; ++w) M = fmaxf(M, s_m[w]);
     const float Mc = (M == -INFINITY) ? 0.f : __fmul_rn(M, P.c);
-    double t = (m == -INFINITY) ? 0.0 : (double)sum * (double)ex2(mc - Mc);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+    // Sums in double-float: a dependent fp64 operation costs about 14 fp32
+    // ones on this part.
+    DF t = (m == -INFINITY) ? DF{0.f, 0.f} : df_mul_f(DF{sum, 0.f}, ex2(mc - Mc));
+    t = warp_sum_df(t);
     if (lane == 0) s_S[warp] = t;
     __syncthreads();
     if (tid == 0) {
-      double S = 0.0;
+      DF Sd = s_S[0];
       float bv = s_av[0];
       int bi = s_ai[0];
-      for (int w = 0; w < kW; ++w) {
-        S += s_S[w];
+      for (int w = 1; w < kW; ++w) {
+        Sd = df_add(Sd, s_S[w]);
         argmax_merge(bv, bi, s_av[w], s_ai[w]);
       }
+      const double S = df_to_d(Sd);
       sv_shard_stat st;
       st.mc = Mc;
       st.zx = s_zx;
@@ -381,19 +425,17 @@ __device__ __forceinline__ void residual(const Job& J, int kind, float c, float 
   }
 }
 
-// Sums of r over each tile of kT * EPV elements of the slice, in fp64, into
-// tt[0, ntiles) (shared); per thread fp32 over its EPV elements, per warp
-// fp32, over the warps fp64 in warp order.
+// Sums of r over each tile of kT * EPV elements of the slice, in
+// double-float, into tt[0, ntiles) (shared); per thread fp32 over its EPV
+// elements, per warp fp32, over the warps double-float in warp order. The
+// 16-byte path keeps kU tiles' loads in flight before using any.
 template <int DT, bool VEC>
 __device__ void tile_totals(const Slice& sl, const Job& J, int kind, float c, float bhi, float blo,
-                            float* wt, double* tt, int ntiles) {
+                            float* wt, DF* tt, int ntiles) {
   constexpr int EPV = Elem<DT>::kEPV;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int l = 0; l < ntiles; ++l) {
-    const int e = l * kT * EPV + tid * EPV;
-    float zp[EPV], zq[EPV], r[EPV];
-    load_elems<DT, VEC>(sl.p, e, sl.Vs, zp);
-    if (kind == kResidual) load_elems<DT, VEC>(sl.q, e, sl.Vs, zq);
+  auto one = [&](int l, const float (&zp)[EPV], const float (&zq)[EPV], int e) {
+    float r[EPV];
     residual<EPV>(J, kind, c, bhi, blo, zp, zq, sl.v0 + e, r);
     float ts = 0.f;
 #pragma unroll
@@ -401,11 +443,42 @@ __device__ void tile_totals(const Slice& sl, const Job& J, int kind, float c, fl
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ts += __shfl_xor_sync(kFull, ts, o);
     if (lane == 0) wt[l * kW + warp] = ts;
+  };
+  if constexpr (VEC) {
+    constexpr int kU = 4;
+    const uint4 ninf = DT == 1 ? make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u)
+                               : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+    for (int l0 = 0; l0 < ntiles; l0 += kU) {
+      uint4 rp[kU], rq[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int e = (l0 + u) * kT * EPV + tid * EPV;
+        const bool in = l0 + u < ntiles && e < sl.Vs;
+        rp[u] = in ? ld_stream16(sl.p + (size_t)e * Elem<DT>::kBytes) : ninf;
+        rq[u] = (in && kind == kResidual) ? ld_stream16(sl.q + (size_t)e * Elem<DT>::kBytes) : ninf;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        if (l0 + u >= ntiles) break;
+        float zp[EPV], zq[EPV];
+        Elem<DT>::unpack(rp[u], zp);
+        Elem<DT>::unpack(rq[u], zq);
+        one(l0 + u, zp, zq, (l0 + u) * kT * EPV + tid * EPV);
+      }
+    }
+  } else {
+    for (int l = 0; l < ntiles; ++l) {
+      const int e = l * kT * EPV + tid * EPV;
+      float zp[EPV], zq[EPV];
+      load_elems<DT, VEC>(sl.p, e, sl.Vs, zp);
+      if (kind == kResidual) load_elems<DT, VEC>(sl.q, e, sl.Vs, zq);
+      one(l, zp, zq, e);
+    }
   }
   __syncthreads();
   for (int l = tid; l < ntiles; l += kT) {
-    double t = 0.0;
-    for (int w = 0; w < kW; ++w) t += (double)wt[l * kW + w];
+    DF t{0.f, 0.f};
+    for (int w = 0; w < kW; ++w) t = df_add_f(t, wt[l * kW + w]);
     tt[l] = t;
   }
   __syncthreads();
@@ -434,7 +507,7 @@ template <int DT, bool VEC>
 __global__ void __launch_bounds__(kT) mass_kernel(MassParams P) {
   constexpr int EPV = Elem<DT>::kEPV;
   __shared__ float wt[kMaxTiles * kW];
-  __shared__ double tt[kMaxTiles];
+  __shared__ DF tt[kMaxTiles];
   if (!offsets_ok(P.cu, P.B, P.R_t)) return;
   const int ntiles = (P.Vs + kT * EPV - 1) / (kT * EPV);
   for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
@@ -459,10 +532,11 @@ __global__ void __launch_bounds__(kT) mass_kernel(MassParams P) {
     float bhi, blo;
     beta_of(J, bhi, blo);
     tile_totals<DT, VEC>(sl, J, J.kind, P.c, bhi, blo, wt, tt, ntiles);
-    if (threadIdx.x == 0) {
-      double z = 0.0;
-      for (int l = 0; l < ntiles; ++l) z += tt[l];
-      P.mass[b] = z;
+    if (threadIdx.x < 32) {  // the slice's mass: warp 0 sums the tiles in double-float
+      DF z{0.f, 0.f};
+      for (int l = threadIdx.x; l < ntiles; l += 32) z = df_add(z, tt[l]);
+      z = warp_sum_df(z);
+      if (threadIdx.x == 0) P.mass[b] = df_to_d(z);
     }
     __syncthreads();
   }
@@ -490,10 +564,10 @@ __global__ void __launch_bounds__(kT) draw_kernel(DrawParams P) {
   constexpr int EPV = Elem<DT>::kEPV;
   constexpr int TILE = kT * EPV;
   __shared__ float wt[kMaxTiles * kW];
-  __shared__ double tt[kMaxTiles], tincl[kMaxTiles], dred[kW], dred2[kW], wexcl[kW + 1];
+  __shared__ DF tt[kMaxTiles], tincl[kMaxTiles], dred[kW], dred2[kW], wexcl[kW + 1];
   __shared__ float redf[kW];
   __shared__ int s_owner, s_kind, pick, pick2, tok;
-  __shared__ double s_T;
+  __shared__ DF s_T;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (!offsets_ok(P.cu, P.B, P.R_t)) return;
   const int ntiles = (P.Vs + TILE - 1) / TILE;
@@ -541,7 +615,7 @@ __global__ void __launch_bounds__(kT) draw_kernel(DrawParams P) {
       }
       s_owner = owner;
       s_kind = kind;
-      s_T = Tl;
+      s_T = df_from_d(Tl);
       if (owner != P.shard) {
         P.draw_tok[b] = -1;
         P.draw_prob[2 * (size_t)b] = -1.f;
@@ -555,7 +629,7 @@ __global__ void __launch_bounds__(kT) draw_kernel(DrawParams P) {
       continue;
     }
     const int kind = s_kind;
-    const double T = s_T;
+    const DF T = s_T;
     Slice sl;
     sl.p = P.target + (long long)J.row * P.ld_bytes;
     sl.q = J.kind == kResidual ? P.draft + (long long)J.drow * P.ld_bytes : nullptr;
@@ -566,38 +640,30 @@ __global__ void __launch_bounds__(kT) draw_kernel(DrawParams P) {
     float bhi, blo;
     beta_of(Jk, bhi, blo);
     tile_totals<DT, VEC>(sl, Jk, kind, P.c, bhi, blo, wt, tt, ntiles);
-    // The tile holding T: the last tile with mass whose lower edge is <= T.
-    const double mine = tid < ntiles ? tt[tid] : 0.0;
-    double inc = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double u = __shfl_up_sync(kFull, inc, o);
-      if (lane >= o) inc += u;
-    }
+    // The tile holding T: the last tile with mass whose lower edge is <= T
+    // (scans in double-float).
+    const DF mine = tid < ntiles ? tt[tid] : DF{0.f, 0.f};
+    const DF inc = warp_incl_scan_df(mine, lane);
     if (lane == 31) dred[warp] = inc;
     __syncthreads();
     if (warp == 0) {
-      double v = lane < kW ? dred[lane] : 0.0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double u = __shfl_up_sync(kFull, v, o);
-        if (lane >= o) v += u;
-      }
+      DF v = lane < kW ? dred[lane] : DF{0.f, 0.f};
+      v = warp_incl_scan_df(v, lane);
       if (lane < kW) dred2[lane] = v;
     }
     __syncthreads();
-    if (tid < ntiles) tincl[tid] = inc + (warp > 0 ? dred2[warp - 1] : 0.0);
+    if (tid < ntiles) tincl[tid] = warp > 0 ? df_add(dred2[warp - 1], inc) : inc;
     if (tid == 0) pick = -1;
     __syncthreads();
     if (tid < ntiles) {
-      const double lo = tid ? tincl[tid - 1] : 0.0;
-      if (mine > 0.0 && lo <= T) atomicMax(&pick, tid);
+      const DF lo = tid ? tincl[tid - 1] : DF{0.f, 0.f};
+      if (df_pos(mine) && df_le(lo, T)) atomicMax(&pick, tid);
     }
     __syncthreads();
     const int kt = pick;
     int y = -1;
     if (kt >= 0) {
-      const double Tk = T - (kt ? tincl[kt - 1] : 0.0);
+      const DF Tk = kt ? df_sub(T, tincl[kt - 1]) : T;
       const int e = kt * TILE + tid * EPV;
       float zp[EPV], zq[EPV], r[EPV];
       load_elems<DT, VEC>(sl.p, e, sl.Vs, zp);
@@ -612,26 +678,26 @@ __global__ void __launch_bounds__(kT) draw_kernel(DrawParams P) {
       if (lane == 31) redf[warp] = incl;
       __syncthreads();
       if (tid == 0) {
-        double a = 0.0;
-        wexcl[0] = 0.0;
+        DF a{0.f, 0.f};
+        wexcl[0] = a;
         for (int w = 0; w < kW; ++w) {
-          a += (double)redf[w];
+          a = df_add_f(a, redf[w]);
           wexcl[w + 1] = a;
         }
         pick2 = -1;
         tok = -1;
       }
       __syncthreads();
-      const double lo = wexcl[warp] + (double)lane_lo;
-      if (ts > 0.f && lo <= Tk) atomicMax(&pick2, tid);
+      const DF lo = df_add_f(wexcl[warp], lane_lo);
+      if (ts > 0.f && df_le(lo, Tk)) atomicMax(&pick2, tid);
       __syncthreads();
       if (tid == pick2) {
-        double run = lo;
+        DF run = lo;
         int cand = e;
 #pragma unroll
         for (int j = 0; j < EPV; ++j) {
-          if (r[j] > 0.f && run <= Tk) cand = e + j;
-          run += (double)r[j];
+          if (r[j] > 0.f && df_le(run, Tk)) cand = e + j;
+          run = df_add_f(run, r[j]);
         }
         tok = cand;
       }
