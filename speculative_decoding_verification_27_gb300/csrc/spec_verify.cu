@@ -122,7 +122,7 @@ constexpr int max_vocab(int dtype) { return kMaxScanTiles * kThreads * (dtype ==
 #define SV_MINBLOCKS 3
 #endif
 #ifndef SV_PART_CHUNKS
-#define SV_PART_CHUNKS 4
+#define SV_PART_CHUNKS 1
 #endif
 #ifndef SV_PUBLISH_PCT
 #define SV_PUBLISH_PCT 0
@@ -1255,10 +1255,10 @@ __device__ __noinline__ bool commit_request(const Params& P, Smem& s, unsigned c
   if (tid == 0) {
     constexpr int TILE = kThreads * Elem<DT & 1>::kEPV;
     const int nchunks = ((P.V + TILE - 1) / TILE + kVPT - 1) / kVPT;
-    // When every request's draw, cut into single chunks, fits in one wave of
-    // CTAs (a small batch), use single-chunk parts; otherwise larger ones.
-    int nparts = (long long)P.B * nchunks <= (long long)gridDim.x
-                     ? nchunks : (nchunks + kPartChunks - 1) / kPartChunks;
+    // Draws published here come due after the last rows are handed out, when
+    // CTAs fall idle: single-chunk parts spread them widest (kPartChunks; 4
+    // measured 0.6% slower on the benchmark batch), up to kMaxParts.
+    int nparts = (nchunks + kPartChunks - 1) / kPartChunks;
     nparts = nparts > kMaxParts ? kMaxParts : nparts;
     // Parts carry a fixed cost (descriptor, ring start, a global merge); a
     // draw that streams less than kMinPublishBytes is faster kept whole.
