@@ -151,7 +151,10 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
  * §二, strict verification): accept slot i iff x̂_i equals the argmax of
  * target row i (lowest index among ties); at the first mismatch, or at the
  * bonus row, emit that row's argmax. Bit-exact; no temperature, no
- * uniforms. Arguments as for spec_verify.
+ * uniforms. Arguments as for spec_verify. On 16-byte-aligned rows whose
+ * byte length is a multiple of 16, one CTA per target row streams the row
+ * (eight 16-byte loads in flight per thread) and the request's last row
+ * commits it; other rows take the persistent kernel.
  */
 sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype, int32_t V, int32_t B,
                              const int32_t* draft_tokens, const int32_t* cu_draft,
@@ -159,8 +162,8 @@ sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype, int32_t 
                              size_t workspace_bytes, void* cuda_stream);
 
 /*
- * Which kernel runs spec_verify and spec_verify_greedy. Both compute the
- * same step (the rule above):
+ * Which kernel runs spec_verify. Both compute the same step (the rule
+ * above):
  *   - a persistent kernel, a fixed number of CTAs per SM, streams rows
  *     through a shared-memory ring and commits each request as soon as its
  *     stop slot is known; the default for large batches;

@@ -46,6 +46,7 @@
 #include "sv_device.cuh"
 #include "sv_filter.cuh"
 #include "sv_cluster.cuh"
+#include "sv_greedy.cuh"
 
 namespace sv {
 
@@ -2074,6 +2075,24 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
                    (((size_t)V * es) % 16 == 0);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (greedy_all && vec && !thr) {
+    // Strict verification needs only each row's argmax: one CTA per row.
+    GParams G;
+    G.target = target;
+    G.V = V;
+    G.B = B;
+    G.draft_tokens = draft_tokens;
+    G.cu = cu_draft;
+    G.out_tokens = out_tokens;
+    G.out_len = out_len;
+    G.status = &P.ws->status;
+    G.arrive = P.req_state;
+    G.rows = reinterpret_cast<CRow*>(P.rows);
+    G.row_cap = P.row_cap;
+    G.nvec = (int)(((size_t)V * es) / 16);
+    e = launch_greedy_verify(G, dtype == SV_BF16 ? 1 : 0, st);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  }
   if (vec && !thr && P.row_cap <= (long long)g_cluster_rows.load(std::memory_order_relaxed) &&
       cluster_smem_bytes((size_t)V * es, P.draft != nullptr) > 0) {
     CParams C;

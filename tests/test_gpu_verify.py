@@ -340,3 +340,50 @@ def test_cluster_rows_beyond_the_workspace_are_reported(cuda_lib):
         assert api.sv_check_status(ws) == 0
     finally:
         api.sv_set_cluster_rows(prev)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_greedy_entry_ties_empty_rows_and_two_lookup_rounds(cuda_lib, dtype):
+    """spec_verify_greedy on 16-byte vector rows runs the one-CTA-per-row
+    greedy kernel: logits on a coarse grid (ties: the lowest index wins),
+    rows of -inf only (index 0), requests with K = 0, an out-of-range token,
+    and B = 300 > 256 requests (two rounds of the request lookup)."""
+    rng = np.random.default_rng(730)
+    B, V = 300, 1024
+    Ks = rng.integers(0, 6, B).astype(np.int32)
+    cu = np.concatenate([[0], np.cumsum(Ks)]).astype(np.int32)
+    R_t = int(cu[-1]) + B
+    zt = (np.round(rng.normal(0, 1.5, (R_t, V)) * 2) / 2).astype(np.float32)
+    zt[rng.choice(R_t, 7, replace=False)] = -np.inf
+    am = np.argmax(zt, axis=1)  # first index of the maximum (0 for -inf rows)
+    toks = np.empty(int(cu[-1]), np.int32)
+    for b_ in range(B):
+        for i in range(Ks[b_]):
+            row = cu[b_] + b_ + i
+            toks[cu[b_] + i] = am[row] if rng.random() < 0.75 else rng.integers(V)
+    bad = toks.size // 2
+    b_bad = int(np.searchsorted(cu, bad, side="right") - 1)
+    toks_ora = toks.copy()  # the oracle refuses an out-of-range token: any mismatch stands in
+    toks_ora[bad] = (am[bad + b_bad] + 1) % V
+    toks[bad] = V + 5  # out of range: a mismatch, and a status bit
+    mode = np.full(B, 1, np.uint8)
+    zstore = W.to_bf16_bits(zt) if dtype == "bf16" else zt
+    b = W.VerifyBatch("greedy_edges", zstore, None, toks, cu, W.uniforms_for(cu, 11), 1.0, mode)
+    db = parity.to_device(b)
+    ws = api.new_workspace(b.B, b.R_t, b.V)
+    tok, ln = api.spec_verify_greedy(db.target, db.draft_tokens, db.cu_draft, workspace=ws)
+    torch.cuda.synchronize()
+    assert api.sv_check_status(ws) == api.SV_DATA_BAD_TOKEN
+    ora = parity.oracle_verify(W.VerifyBatch("greedy_edges", zstore, None, toks_ora, cu, b.uniforms, 1.0, mode))
+    tok, ln = tok.cpu().numpy(), ln.cpu().numpy()
+    assert np.array_equal(ln, ora.out_len)
+    t0 = b.cu_draft[:-1] + np.arange(b.B)
+    for i in range(b.B):
+        n = ln[i]
+        want = ora.out_tokens[t0[i]:t0[i] + n].copy()
+        if cu[i] <= bad < cu[i + 1] and bad - cu[i] < n - 1:
+            want[bad - cu[i]] = V + 5  # not reached: the bad slot rejects, so it is never committed
+        assert np.array_equal(tok[t0[i]:t0[i] + n], want), i
+    tok2, ln2 = api.spec_verify_greedy(db.target, db.draft_tokens, db.cu_draft, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(ln2.cpu(), torch.from_numpy(ln)) and api.sv_check_status(ws) == api.SV_DATA_BAD_TOKEN
