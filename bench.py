@@ -664,6 +664,11 @@ def _extra_setup(name, seed):
             "temperature": b0.temperature, "input_sets": len(batches)}
     if filtered:
         desc.update({"top_k": FILTER_K, "top_p": FILTER_P})
+    # Kernels of this library per step: the filtered step runs the one-warp
+    # and CTA threshold kernels, the filtered commit and the verify kernel;
+    # the sharded step two statistics kernels per shard, the decisions, a
+    # mass and a draw kernel per shard and the finish.
+    desc["launches_per_step"] = {"topkp_b256": 4, "vshard_b256x2": 10, "candidates_b64x4": 2}.get(name, 1)
     outs = [ot, ol] if not cands else [ot, ol, best, best_len]
     if sharded:
         desc.update({"shards": 2, "shard_bounds": bounds, "launch": "the step captured once in a CUDA graph, replayed"})
@@ -751,7 +756,7 @@ def run_extra(args):
                               "metrics_b512": "latency-bound: 4 KB of inputs"}.get(args.workload)},
         "e2e": {"value": units / (e_ms * 1e-3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e_ms},
-        "gpu_launches": n,
+        "gpu_launches": n * desc.get("launches_per_step", 1),
         "clocks": clocks,
         "cpu_baseline": {"value": (units if args.workload in ("ngram_b128", "suffix_b128", "verify_b1", "greedy_b64",
                                                             "onehot_b128", "metrics_b512")

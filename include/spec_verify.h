@@ -98,8 +98,10 @@ enum { SV_MODE_SAMPLE = 0, SV_MODE_GREEDY = 1 };
  * for up to min(B, 4096) final draws it splits the same way, a descriptor and
  * the partial sums of each. It must be 16-byte aligned and zero-filled
  * before its first use; every call leaves its counters at zero again, so
- * calls in stream order may reuse it without clearing. Calls that may run
- * concurrently (other streams) need distinct workspaces.
+ * calls in stream order with the same B and V (the layout) may reuse it
+ * without clearing. A call with another B or V needs it zero-filled again:
+ * the counters then sit where the last call left other data. Calls that may
+ * run concurrently (other streams) need distinct workspaces.
  */
 size_t spec_verify_workspace_size(int32_t B, int32_t R_t, int32_t V);
 
@@ -211,7 +213,8 @@ int32_t sv_set_cluster_rows(int32_t rows);
  *              thresholds occupy the start of the workspace.
  *   top_k, top_p  the filters (top_k >= 0, top_p > 0).
  *   workspace  >= spec_verify_filtered_workspace_size(B, R_t, V) bytes,
- *              16-byte aligned, zero-filled before first use.
+ *              16-byte aligned, zero-filled before first use and again
+ *              before a call with another B, R_t or V (the layout).
  * Per row, the threshold step finds the row's threshold:
  *   - top-k up to 128 on 16-byte-aligned rows whose width is a multiple of
  *     16 bytes: one warp per row reads the row once, collects the logits
@@ -228,9 +231,16 @@ int32_t sv_set_cluster_rows(int32_t rows);
  *     top-p alone, the row is read once; rows whose candidates do not fit
  *     (long tie groups at the threshold, or flat rows under top-p) and
  *     larger k take several passes over the row.
- * The verify kernel then counts every logit below its row's threshold as
- * -inf. A top-p decision within about 1e-6 of its boundary can differ from
- * a float64 evaluation.
+ * The verify step then counts every logit below its row's threshold as
+ * -inf. When the one-warp-per-row kernel ran, a commit kernel with one CTA
+ * per request comes next: for a sampled request with K <= 31 whose rows all
+ * carry their statistics and whose stop row its kept list, it decides every
+ * slot from z(x̂) alone, draws from the stop row's list and commits, without
+ * reading any row again. The verify kernel then runs only for the requests
+ * it left (greedy ones, larger K, rows without statistics or list), and
+ * returns at once when there are none. Both take the same decisions in the
+ * same arithmetic, so the split changes no output. A top-p decision within
+ * about 1e-6 of its boundary can differ from a float64 evaluation.
  */
 size_t spec_verify_filtered_workspace_size(int32_t B, int32_t R_t, int32_t V);
 sv_status spec_verify_filtered(const void* target_logits, const void* draft_logits,

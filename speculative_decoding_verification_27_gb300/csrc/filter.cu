@@ -928,6 +928,8 @@ template <int DT>
 __global__ void __launch_bounds__(kFtThreads, 3) threshold_kernel(FtParams P) {
   extern __shared__ __align__(16) unsigned char ft_smem[];
   FtSmem& s = *reinterpret_cast<FtSmem*>(ft_smem);
+  // The warp kernel finished every row: nothing to do.
+  if (P.after_warp && P.rows_left && __ldcg(P.rows_left) == 0u) return;
   // Rows past the caller's arrays (offsets that the verify kernel will
   // reject) are skipped.
   int R_d = P.cu[P.B], R_t = R_d + P.B;
@@ -993,7 +995,24 @@ __global__ void __launch_bounds__(kFtThreads, 3) threshold_kernel(FtParams P) {
 constexpr int kWarpMaxK = 128;
 constexpr int kWTop = 4;          // vector maxima each lane tracks: k <= 32 * kWTop
 constexpr int kWCap = 512;        // logits a warp's buffer holds
-constexpr int kWLoads = 8;        // 16-byte vectors a lane has in flight
+#ifndef SV_WLOADS
+#define SV_WLOADS 8
+#endif
+constexpr int kWLoads = SV_WLOADS;  // 16-byte vectors a lane has in flight
+#ifndef SV_WWARPS
+#define SV_WWARPS 4
+#endif
+// Rows (warps) per CTA of the warp kernel. The rows of a batch make about
+// one wave of warps; small CTAs spread them evenly over the SMs (on 3840
+// rows of 151936 bf16 logits: 8 per CTA 259 µs per filtered call, 4 248 µs,
+// 2 249 µs, 1 305 µs).
+constexpr int kWWarps = SV_WWARPS;
+constexpr int kWThreads = 32 * kWWarps;
+#ifndef SV_WMINB
+#define SV_WMINB (32 / SV_WWARPS)
+#endif
+constexpr int kWMinBlocks = SV_WMINB;  // resident CTAs per SM the register budget allows
+
 static_assert(kWarpMaxK <= 32 * kWTop, "k of the tracked maxima must exist");
 
 // 16-byte streaming load that does not allocate in L1 (read once).
@@ -1056,13 +1075,13 @@ __device__ __forceinline__ float value_of_key(uint32_t k) {
 }
 
 struct WarpRowSmem {
-  float buf[kFtWarps][kWCap];  // buffered logits
-  int ix[kFtWarps][kWCap];     // their tokens
-  unsigned n[kFtWarps];
+  float buf[kWWarps][kWCap];  // buffered logits
+  int ix[kWWarps][kWCap];     // their tokens
+  unsigned n[kWWarps];
 };
 
 template <int DT>
-__global__ void __launch_bounds__(kFtThreads, 4) threshold_warp_kernel(FtParams P) {
+__global__ void __launch_bounds__(kWThreads, kWMinBlocks) threshold_warp_kernel(FtParams P) {
   constexpr int EV = DT == 1 ? 8 : 4;  // logits per 16-byte vector
   __shared__ WarpRowSmem sm;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1076,7 +1095,7 @@ __global__ void __launch_bounds__(kFtThreads, 4) threshold_warp_kernel(FtParams 
   const int k = P.top_k;
   const bool use_p = P.top_p > 0.f && P.top_p < 1.f;
   const int nvec = P.V / EV;
-  for (int r = blockIdx.x * kFtWarps + warp; r < rows; r += gridDim.x * kFtWarps) {
+  for (int r = blockIdx.x * kWWarps + warp; r < rows; r += gridDim.x * kWWarps) {
     const bool is_t = r < R_t;
     const int rr = is_t ? r : r - R_t;
     int greedy = 0;
@@ -1276,6 +1295,7 @@ __global__ void __launch_bounds__(kFtThreads, 4) threshold_warp_kernel(FtParams 
       // Rows left with ok = 0 get their threshold from the CTA kernel.
       if (out.ok || greedy) (is_t ? P.thr_t : P.thr_d)[rr] = tau;
       (is_t ? P.fst_t : P.fst_d)[rr] = out;
+      if (!out.ok && !greedy && P.rows_left) *P.rows_left = 1u;  // the CTA kernel has work
     }
     __syncwarp();
   }
@@ -1299,7 +1319,8 @@ static cudaError_t launch_thresholds_t(const FtParams& P, int sms, cudaStream_t 
   return cudaGetLastError();
 }
 
-cudaError_t launch_thresholds(const FtParams& P0, int dtype, cudaStream_t st) {
+cudaError_t launch_thresholds(const FtParams& P0, int dtype, cudaStream_t st, bool* warp_ran) {
+  *warp_ran = false;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1311,15 +1332,16 @@ cudaError_t launch_thresholds(const FtParams& P0, int dtype, cudaStream_t st) {
   // kernel then takes only the rows it left.
   if (P.fst_t && P.vec && P.top_k >= 1 && P.top_k <= kWarpMaxK) {
     const int rows = 2 * P.rows_t;
-    int grid = (rows + kFtWarps - 1) / kFtWarps;
+    int grid = (rows + kWWarps - 1) / kWWarps;
     if (grid < 1) grid = 1;
     if (dtype == SV_BF16)
-      threshold_warp_kernel<1><<<grid, kFtThreads, 0, st>>>(P);
+      threshold_warp_kernel<1><<<grid, kWThreads, 0, st>>>(P);
     else
-      threshold_warp_kernel<0><<<grid, kFtThreads, 0, st>>>(P);
+      threshold_warp_kernel<0><<<grid, kWThreads, 0, st>>>(P);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     P.after_warp = true;
+    *warp_ran = true;
   }
   return dtype == SV_BF16 ? launch_thresholds_t<1>(P, sms, st) : launch_thresholds_t<0>(P, sms, st);
 }

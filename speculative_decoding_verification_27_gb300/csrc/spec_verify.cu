@@ -201,6 +201,8 @@ struct Params {
   const FStat* fst;         // [R_t] filtered softmax statistics of the target rows, or NULL
   const FStat* fst_d;       // [R_d] of the draft rows, or NULL
   const int2* flist;        // [R_t, kKeptListCap] kept (token, logit bits) per target row, or NULL
+  unsigned* fc_need;        // the filtered commit left requests (nonzero), or NULL: no such commit ran
+  const unsigned char* fc_done;  // [B] 1: request committed by the filtered commit
   int n_slots, tsum_stride;
   unsigned int* part_done;  // [kMaxTailRows] parts finished per split row
   PartRec* parts;           // [kMaxPartRecs]
@@ -1697,6 +1699,13 @@ __device__ bool process_item(const Params& P, Smem& s, unsigned char* ring, int 
   if (tid < 32) row_meta(P, s, o, bq);
   __syncthreads();
   const int b = s.b, t = s.t, t0 = s.t0, d0 = s.d0, K = s.K, i = s.i;
+  if constexpr ((DT & kFilt) != 0) {
+    if (P.fc_done && P.fc_done[b]) {
+      // Committed by the filtered commit: counted once, by its first row.
+      if (tid == 0 && i == 0 && part <= 0) atomicAdd(&P.ws->committed, 1u);
+      return true;
+    }
+  }
   const bool greedy = s.greedy != 0;
   const size_t rowb = (size_t)P.V * Elem<DT & 1>::kBytes;
   const char* trow = static_cast<const char*>(P.target) + (size_t)t * rowb;
@@ -1794,6 +1803,8 @@ __global__ void __launch_bounds__(kThreads, SV_MINBLOCKS) verify_kernel(Params P
   __shared__ Smem s;
   extern __shared__ __align__(128) unsigned char ring[];
   const int tid = threadIdx.x;
+  // The filtered commit finished every request: nothing is left.
+  if ((DT & kFilt) != 0 && P.fc_need && __ldcg(P.fc_need) == 0u) return;
   // Offsets must be a valid packed layout that fits the workspace; every CTA
   // checks and all of them take the same decision.
   bool bad = false;
@@ -1905,6 +1916,7 @@ __global__ void __launch_bounds__(kThreads, SV_MINBLOCKS) verify_kernel(Params P
     P.ws->draw_head = 0u;
     P.ws->committed = 0u;
     P.ws->exited = 0u;
+    if (P.fc_need) *P.fc_need = 0u;  // every CTA read it on entry
   }
 }
 
@@ -2023,7 +2035,7 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
                             int greedy_all, const float* thr = nullptr,
                             const float* thr_d = nullptr, const FStat* fst = nullptr,
                             const FStat* fst_d = nullptr, const int2* flist = nullptr,
-                            int row_tiles = 1) {
+                            int row_tiles = 1, FcParams* fc = nullptr) {
   const sv_status chk = check_verify_args(target, draft, dtype, V, B, draft_tokens, cu_draft, uniforms,
                                           temperature, out_tokens, out_len, out_probs, greedy_all);
   if (chk != SV_OK || B == 0) return chk;
@@ -2069,6 +2081,8 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
   P.fst = fst;
   P.fst_d = fst_d;
   P.flist = flist;
+  P.fc_need = nullptr;
+  P.fc_done = nullptr;
 
   // Bulk copies need 16-byte aligned row starts and 16-byte multiples.
   const bool vec = ((uintptr_t)target % 16 == 0) && (!P.draft || (uintptr_t)P.draft % 16 == 0) &&
@@ -2119,6 +2133,19 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
   }
   if (thr) {
+    if (fc) {
+      // Requests whose rows all carry their statistics are decided, drawn
+      // and committed first, one CTA each; the verify kernel takes the rest.
+      fc->out_tokens = out_tokens;
+      fc->out_len = out_len;
+      fc->out_probs = P.out_probs;
+      fc->status = &P.ws->status;
+      if (fc->rows_t > P.row_cap) fc->rows_t = (int)P.row_cap;
+      e = launch_filtered_commit(*fc, dtype == SV_BF16 ? 1 : 0, st);
+      if (e != cudaSuccess) return SV_ERR_CUDA;
+      P.fc_need = fc->need_slow;
+      P.fc_done = fc->done;
+    }
     if (dtype == SV_BF16)
       e = vec ? launch<1 | kFilt, true>(P, st) : launch<1 | kFilt, false>(P, st);
     else
@@ -2199,9 +2226,12 @@ static size_t filter_thr_bytes(int64_t R_t, int64_t B) {
 static size_t filter_fst_bytes(int64_t R_t, int64_t B) {
   return (size_t)R_t * sizeof(sv::FStat) + (size_t)(R_t - B + 1) * sizeof(sv::FStat);
 }
+static size_t filter_list_bytes(int64_t R_t) { return (size_t)R_t * sv::kKeptListCap * sizeof(int2); }
+// Flags of the filtered commit: rows left to the CTA threshold kernel,
+// requests left to the verify kernel, then one "committed" byte per request.
+static size_t filter_flag_bytes(int64_t B) { return sv::align16(8 + (size_t)B); }
 static size_t filter_bytes(int64_t R_t, int64_t B) {
-  return filter_thr_bytes(R_t, B) + filter_fst_bytes(R_t, B) +
-         (size_t)R_t * sv::kKeptListCap * sizeof(int2);
+  return filter_thr_bytes(R_t, B) + filter_fst_bytes(R_t, B) + filter_list_bytes(R_t) + filter_flag_bytes(B);
 }
 
 size_t spec_verify_filtered_workspace_size(int32_t B, int32_t R_t, int32_t V) {
@@ -2251,13 +2281,38 @@ sv_status spec_verify_filtered(const void* target_logits, const void* draft_logi
   fp.fst_t = reinterpret_cast<sv::FStat*>(ws + filter_thr_bytes(R_t, B));
   fp.fst_d = fp.fst_t + R_t;
   fp.list_t = reinterpret_cast<int2*>(ws + filter_thr_bytes(R_t, B) + filter_fst_bytes(R_t, B));
+  unsigned* flags = reinterpret_cast<unsigned*>(ws + filter_thr_bytes(R_t, B) + filter_fst_bytes(R_t, B) +
+                                                filter_list_bytes(R_t));
+  fp.rows_left = flags;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  if (sv::launch_thresholds(fp, dtype, st) != cudaSuccess) return SV_ERR_CUDA;
+  bool warp_ran = false;
+  if (sv::launch_thresholds(fp, dtype, st, &warp_ran) != cudaSuccess) return SV_ERR_CUDA;
+  // The one-warp-per-row thresholds leave statistics and kept lists that
+  // let most requests commit without the verify kernel.
+  sv::FcParams fc;
+  fc.target = target_logits;
+  fc.draft = draft_logits;
+  fc.V = V;
+  fc.B = B;
+  fc.rows_t = R_t;
+  fc.draft_tokens = draft_tokens;
+  fc.cu = cu_draft;
+  fc.mode = mode;
+  fc.uniforms = uniforms;
+  fc.c = fp.c;
+  fc.thr_t = fp.thr_t;
+  fc.thr_d = draft_logits ? fp.thr_d : nullptr;
+  fc.fst_t = fp.fst_t;
+  fc.fst_d = draft_logits ? fp.fst_d : nullptr;
+  fc.list_t = fp.list_t;
+  fc.need_slow = flags + 1;
+  fc.done = reinterpret_cast<unsigned char*>(flags + 2);
+  fc.rows_left = flags;
   return sv::run_verify(target_logits, draft_logits, dtype, V, B, draft_tokens, cu_draft, mode,
                         uniforms, temperature, out_tokens, out_len, out_probs, ws + fb,
                         workspace_bytes - fb, cuda_stream, 0, fp.thr_t,
                         draft_logits ? fp.thr_d : nullptr, fp.fst_t, draft_logits ? fp.fst_d : nullptr,
-                        fp.list_t);
+                        fp.list_t, 1, warp_ran ? &fc : nullptr);
 }
 
 size_t spec_verify_workspace_size(int32_t B, int32_t R_t, int32_t V) {

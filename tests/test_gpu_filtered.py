@@ -248,3 +248,39 @@ def test_listed_rows_degenerate_residual_and_one_hot(cuda_lib, dtype):
     b.draft = None
     rep = _run(b, k, 1.0)
     assert rep.mismatched_requests == 0, rep.as_dict()
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("one_hot", [False, True])
+def test_filtered_commit_and_verify_share_a_batch(cuda_lib, dtype, one_hot):
+    """With the one-warp thresholds, requests whose rows all carry their
+    statistics commit in one CTA each; greedy requests and those with more
+    than 31 drafts go to the verify kernel, which skips the others. A mixed
+    batch, then one the commit takes whole (the verify kernel leaves at
+    once), then the mixed one again, all on one workspace: every call
+    matches the oracle and the two mixed calls are bit-identical."""
+    import oracle
+    V, k, p = 8200, 20, 0.9
+    Ks = [0, 1, 7, 31, 32, 40, 3, 5, 2, 33, 6, 4]
+    mixed = W.gaussian_sampling(seed=590, B=len(Ks), K=Ks, V=V, sigma=2.0, draft_sigma=0.5, T=0.9, dtype=dtype)
+    mixed.mode = np.array([0, 0, 1, 0, 0, 0, 1, 0, 0, 0, 0, 1], np.uint8)
+    # Same B and R_t (one workspace layout), every request sampled with K <= 31.
+    whole = W.gaussian_sampling(seed=591, B=len(Ks), K=[31, 31, 31, 31, 20, 5, 5, 3, 3, 2, 1, 1], V=V,
+                                sigma=2.0, draft_sigma=0.5, T=0.9, dtype=dtype)
+    assert whole.R_t == mixed.R_t
+    if one_hot:
+        mixed.draft = whole.draft = None
+    ws = torch.zeros(api.spec_verify_filtered_workspace_size(mixed.B, mixed.R_t, V), dtype=torch.uint8,
+                     device="cuda")
+    outs = []
+    for b in (mixed, whole, mixed):
+        db = parity.to_device(b)
+        tok, ln, pr = api.spec_verify_filtered(db.target, db.draft, db.draft_tokens, db.cu_draft, db.uniforms,
+                                               db.temperature, k, p, db.mode, workspace=ws)
+        torch.cuda.synchronize()
+        ora = oracle.spec_verify(b.target, b.draft, b.draft_tokens, b.cu_draft, b.uniforms, b.temperature,
+                                 b.mode, top_k=k, top_p=p)
+        rep = parity.compare(b, (tok.cpu().numpy(), ln.cpu().numpy(), pr.cpu().numpy()), ora)
+        assert rep.mismatched_requests == 0, rep.as_dict()
+        outs.append((tok, ln, pr))
+    assert all(torch.equal(x, y) for x, y in zip(outs[0], outs[2]))
