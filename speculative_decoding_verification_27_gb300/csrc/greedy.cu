@@ -10,8 +10,8 @@
 // in flight per thread (no shared-memory ring, no barrier inside the pass),
 // 64 KB per CTA, so that even a batch with fewer rows than twice the SMs
 // keeps the memory busy (8 loads: 25.2 µs on a 64-request batch, 16: 25.0). The row's address needs only
-// cu_draft[B] (for R_t), read with the offsets check at the start; the
-// request lookup runs while the first loads are in flight. The CTA writes
+// cu_draft[B] (for R_t): the first loads go out before the rest of the
+// offsets check, and the request lookup runs while they are in flight. The CTA writes
 // the row's argmax and sets its bits in the request's progress word (one
 // "done" bit per row, one "accepted" bit per draft slot, for K <= 31); the
 // request's last row reads the stop slot off the word and commits. No CTA
@@ -80,26 +80,30 @@ __global__ void __launch_bounds__(kThreads) greedy_verify_kernel(GParams P) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t = blockIdx.x;
 
-  // Offsets: every CTA checks and all take the same decision.
-  bool bad = false;
-  for (int k = tid; k < P.B; k += kThreads)
-    if (P.cu[k + 1] < P.cu[k]) bad = true;
-  if (tid == 0 && (P.cu[0] != 0 || (long long)P.cu[P.B] + P.B > P.row_cap)) bad = true;
-  if (__syncthreads_or(bad)) {
-    if (blockIdx.x == 0 && tid == 0) atomicOr(P.status, SV_DATA_BAD_OFFSETS);
-    return;
-  }
-  if (t >= P.cu[P.B] + P.B) return;
-
-  // The first kU loads of the row go out before the request lookup.
+  // Offsets: every CTA checks and all take the same decision. The row's
+  // first loads need only R_t = cu[B] + B (the rows the layout claims,
+  // within the workspace): they go out before the rest of the check.
+  const int R_d = P.cu[P.B];
+  const long long R_t = (long long)R_d + P.B;
+  const bool rows_ok = R_d >= 0 && R_t <= P.row_cap;
+  const bool live = rows_ok && t < R_t;
   const uint4* row = reinterpret_cast<const uint4*>(static_cast<const char*>(P.target) + (size_t)t * P.nvec * 16);
   const int stride = kThreads * kU;  // vectors per pass of the CTA
   uint4 raw[kU];
 #pragma unroll
   for (int u = 0; u < kU; ++u) {
     const int v = u * kThreads + tid;
-    raw[u] = v < P.nvec ? ld_stream16(row + v) : neg_inf_vec<DT>();
+    raw[u] = (live && v < P.nvec) ? ld_stream16(row + v) : neg_inf_vec<DT>();
   }
+  bool bad = !rows_ok;
+  for (int k = tid; k < P.B; k += kThreads)
+    if (P.cu[k + 1] < P.cu[k]) bad = true;
+  if (tid == 0 && P.cu[0] != 0) bad = true;
+  if (__syncthreads_or(bad)) {
+    if (blockIdx.x == 0 && tid == 0) atomicOr(P.status, SV_DATA_BAD_OFFSETS);
+    return;
+  }
+  if (!live) return;
   const int b = find_request_cta(P.cu, P.B, t);
   if (tid == 0) {
     const int t0 = P.cu[b] + b, d0 = P.cu[b];

@@ -40,6 +40,13 @@ constexpr int kT = kThreads;           // threads per CTA
 constexpr int kW = kT / 32;            // warps per CTA
 constexpr int kMaxTiles = kT;          // one tile per thread in the draw's scan
 constexpr int kStatGrid = 4 * 152;     // CTAs of the row-statistics kernel, at most
+// Tiles whose 16-byte loads (per row of the pair) a thread keeps in flight
+// in the residual-mass and draw passes: one CTA per request streams its two
+// stop-row slices, so the depth sets the pass's bandwidth (4 tiles: 0.378 ms
+// per sharded call on config 3 over two shards, 8: 0.368 ms).
+#ifndef SV_VS_LOADS
+#define SV_VS_LOADS 8
+#endif
 
 static_assert(sizeof(sv_shard_stat) == 32, "shard statistics are 32 bytes");
 
@@ -87,12 +94,15 @@ __device__ __forceinline__ int find_request_cta(const int32_t* cu, int B, int t)
   return lo;
 }
 
-// Offsets of a packed ragged layout are valid for R_t target rows.
+// Offsets of a packed ragged layout are valid for R_t target rows. Every
+// thread of the CTA calls it: each checks a strided share of the pairs and
+// one barrier combines them.
 __device__ __forceinline__ bool offsets_ok(const int32_t* cu, int B, long long R_t) {
-  if (cu[0] != 0) return false;
-  for (int b = 0; b < B; ++b)
-    if (cu[b + 1] < cu[b]) return false;
-  return (long long)cu[B] + B == R_t;
+  bool bad = false;
+  for (int b = threadIdx.x; b < B; b += kT)
+    if (cu[b + 1] < cu[b]) bad = true;
+  if (threadIdx.x == 0 && (cu[0] != 0 || (long long)cu[B] + B != R_t)) bad = true;
+  return !__syncthreads_or(bad);
 }
 
 // ---------------------------------------------------------------------------
@@ -115,19 +125,14 @@ __global__ void __launch_bounds__(kT) stats_kernel(StatParams P) {
   __shared__ float s_m[kW], s_zx;
   __shared__ DF s_S[kW];
   __shared__ float s_av[kW];
-  __shared__ int s_ai[kW], s_x, s_hx, s_ok;
+  __shared__ int s_ai[kW], s_hx;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // Token lookups go through the offsets: they must be a valid layout of
-  // these rows (R_t target rows, or R_d draft rows).
-  if (tid == 0) {
-    bool ok = P.cu[0] == 0;
-    for (int b = 0; b < P.B && ok; ++b) ok = P.cu[b + 1] >= P.cu[b];
-    ok = ok && (P.is_draft ? (long long)P.cu[P.B] == P.rows : (long long)P.cu[P.B] + P.B == P.rows);
-    s_ok = ok;
-    if (!ok && blockIdx.x == 0) atomicOr(P.status, SV_DATA_BAD_OFFSETS);
+  // these rows (R_t target rows, or R_d = R_t - B draft rows).
+  if (!offsets_ok(P.cu, P.B, P.is_draft ? (long long)P.rows + P.B : (long long)P.rows)) {
+    if (blockIdx.x == 0 && tid == 0) atomicOr(P.status, SV_DATA_BAD_OFFSETS);
+    return;
   }
-  __syncthreads();
-  if (!s_ok) return;
   for (int r = blockIdx.x; r < P.rows; r += gridDim.x) {
     // The row's proposed token: draft rows carry their own; target row
     // (b, i) carries draft slot i's when i < K_b (none for the bonus row).
@@ -141,12 +146,12 @@ __global__ void __launch_bounds__(kT) stats_kernel(StatParams P) {
         const int i = r - (P.cu[rb] + rb), K = P.cu[rb + 1] - P.cu[rb];
         x = (i < K && P.tokens) ? P.tokens[P.cu[rb] + i] : -1;
       }
-      s_x = x;
-      s_hx = 0;
-      s_zx = NAN;
+      // The proposed token's logit, if this shard holds it: one load.
+      const char* row = P.logits + (long long)r * P.ld_bytes;
+      const bool here = x >= P.v0 && x < P.v0 + P.Vs;
+      s_zx = here ? Elem<DT>::scalar(row, x - P.v0) : NAN;
+      s_hx = here ? 1 : 0;
     }
-    __syncthreads();
-    const int x = s_x;
     const char* row = P.logits + (long long)r * P.ld_bytes;
     float m = -INFINITY, mc = 0.f, sum = 0.f, av = -INFINITY;
     int ai = INT_MAX;
@@ -161,16 +166,14 @@ __global__ void __launch_bounds__(kT) stats_kernel(StatParams P) {
         mc = nmc;
       }
 #pragma unroll
-      for (int j = 0; j < EPV; ++j) {
-        sum += ex2(fmaf(f[j], P.c, -mc));
-        if (f[j] > av) {  // elements visited in increasing index order
-          av = f[j];
-          ai = P.v0 + e + j;
-        }
-        if (P.v0 + e + j == x) {
-          s_zx = f[j];
-          s_hx = 1;
-        }
+      for (int j = 0; j < EPV; ++j) sum += ex2(fmaf(f[j], P.c, -mc));
+      if (vm > av) {  // elements visited in increasing index order: the first of equal values stays
+#pragma unroll
+        for (int j = 0; j < EPV; ++j)
+          if (f[j] > av) {
+            av = f[j];
+            ai = P.v0 + e + j;
+          }
       }
     };
     if constexpr (VEC) {
@@ -245,7 +248,7 @@ __global__ void __launch_bounds__(kT) stats_kernel(StatParams P) {
 }
 
 // ---------------------------------------------------------------------------
-// 2. Decisions from all shards' statistics (one thread per request)
+// 2. Decisions from all shards' statistics (one warp per request)
 // ---------------------------------------------------------------------------
 struct DecideParams {
   const sv_shard_stat* ts;  // [S, R_t]
@@ -298,69 +301,109 @@ __device__ RowComb combine_row(const sv_shard_stat* st, long long stride, long l
 }
 
 __global__ void __launch_bounds__(kT) decide_kernel(DecideParams P) {
-  const int gt = blockIdx.x * kT + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * kW + (threadIdx.x >> 5), nw = gridDim.x * kW;
   if (!offsets_ok(P.cu, P.B, P.R_t)) {
     // No decision, and no draw for the later kernels to make.
-    if (gt == 0) atomicOr(P.status, SV_DATA_BAD_OFFSETS);
-    for (int b = gt; b < P.B; b += gridDim.x * kT) P.jobs[b].row = -1;
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(P.status, SV_DATA_BAD_OFFSETS);
+    for (int b = blockIdx.x * kT + threadIdx.x; b < P.B; b += gridDim.x * kT) P.jobs[b].row = -1;
     return;
   }
   const long long R_d = P.cu[P.B];
-  for (int b = gt; b < P.B; b += gridDim.x * kT) {
+  // One warp per request: lane i decides draft slot j0 + i; the first
+  // rejection comes from a ballot.
+  for (int b = gw; b < P.B; b += nw) {
     const int d0 = P.cu[b], K = P.cu[b + 1] - d0, t0 = d0 + b;
     int greedy = 0;
     if (P.mode) {
-      if (P.mode[b] == SV_MODE_GREEDY) greedy = 1;
-      else if (P.mode[b] != SV_MODE_SAMPLE) atomicOr(P.status, SV_DATA_BAD_MODE);
+      const uint8_t m = P.mode[b];
+      if (m == SV_MODE_GREEDY) greedy = 1;
+      else if (m != SV_MODE_SAMPLE && lane == 0) atomicOr(P.status, SV_DATA_BAD_MODE);
     }
     int stop = K;
-    for (int i = 0; i < K; ++i) {
-      int x = P.tokens[d0 + i];
-      const bool bad = x < 0 || x >= P.V;
-      if (bad) atomicOr(P.status, SV_DATA_BAD_TOKEN);
-      bool acc;
-      if (greedy) {
-        const RowComb tr = combine_row(P.ts, P.R_t, t0 + i, P.S);
-        const int am = tr.ai == INT_MAX ? 0 : tr.ai;
-        acc = !bad && x == am;
-        if (P.out_probs) {
-          P.out_probs[2 * (size_t)(t0 + i)] = -1.f;
-          P.out_probs[2 * (size_t)(t0 + i) + 1] = -1.f;
-        }
-      } else {
-        // p(x̂) = 2^(z c - Mc_p) / S_p; rho = min(1, p/q), q from the draft
-        // row or 1 for a one-hot proposal; q(x̂) = 0 rejects.
-        const RowComb tr = combine_row(P.ts, P.R_t, t0 + i, P.S);
-        if (!(tr.S > 0.0)) atomicOr(P.status, SV_DATA_EMPTY_ROW);
-        float ph = -1.f, qh = -1.f;
-        acc = false;
-        if (!bad) {
-          const float ap = fmaf(tr.zx, P.c, -tr.Mc);
-          const float pd = __fdiv_rn(exp2f(ap), (float)tr.S);
-          float rho, qd = 1.f;
-          if (P.ds) {
-            const RowComb dr = combine_row(P.ds, R_d, d0 + i, P.S);
-            if (!(dr.S > 0.0)) atomicOr(P.status, SV_DATA_EMPTY_ROW);
-            const float aq = fmaf(dr.zx, P.c, -dr.Mc);
-            qd = __fdiv_rn(exp2f(aq), (float)dr.S);
-            rho = (dr.zx == -INFINITY) ? 0.f
-                                       : fminf(1.f, __fmul_rn(exp2f(ap - aq), __fdiv_rn((float)dr.S, (float)tr.S)));
-          } else {
-            rho = fminf(1.f, pd);
+    for (int j0 = 0; j0 < K; j0 += 32) {
+      const int i = j0 + lane;
+      bool rej = false;
+      if (i < K) {
+        const int x = P.tokens[d0 + i];
+        const bool bad = x < 0 || x >= P.V;
+        if (bad) atomicOr(P.status, SV_DATA_BAD_TOKEN);
+        bool acc;
+        if (greedy) {
+          const RowComb tr = combine_row(P.ts, P.R_t, t0 + i, P.S);
+          const int am = tr.ai == INT_MAX ? 0 : tr.ai;
+          acc = !bad && x == am;
+        } else {
+          // p(x̂) = 2^(z c - Mc_p) / S_p; rho = min(1, p/q), q from the draft
+          // row or 1 for a one-hot proposal; q(x̂) = 0 rejects.
+          const RowComb tr = combine_row(P.ts, P.R_t, t0 + i, P.S);
+          if (!(tr.S > 0.0)) atomicOr(P.status, SV_DATA_EMPTY_ROW);
+          float ph = -1.f, qh = -1.f;
+          acc = false;
+          if (!bad) {
+            const float ap = fmaf(tr.zx, P.c, -tr.Mc);
+            const float pd = __fdiv_rn(exp2f(ap), (float)tr.S);
+            float rho, qd = 1.f;
+            if (P.ds) {
+              const RowComb dr = combine_row(P.ds, R_d, d0 + i, P.S);
+              if (!(dr.S > 0.0)) atomicOr(P.status, SV_DATA_EMPTY_ROW);
+              const float aq = fmaf(dr.zx, P.c, -dr.Mc);
+              qd = __fdiv_rn(exp2f(aq), (float)dr.S);
+              rho = (dr.zx == -INFINITY) ? 0.f
+                                         : fminf(1.f, __fmul_rn(exp2f(ap - aq), __fdiv_rn((float)dr.S, (float)tr.S)));
+            } else {
+              rho = fminf(1.f, pd);
+            }
+            acc = P.uniforms[2 * (size_t)(t0 + i)] < rho;
+            ph = pd;
+            qh = qd;
           }
-          acc = P.uniforms[2 * (size_t)(t0 + i)] < rho;
-          ph = pd;
-          qh = qd;
+          if (P.out_probs) {
+            P.out_probs[2 * (size_t)(t0 + i)] = ph;
+            P.out_probs[2 * (size_t)(t0 + i) + 1] = qh;
+          }
         }
-        if (P.out_probs) {
-          P.out_probs[2 * (size_t)(t0 + i)] = ph;
-          P.out_probs[2 * (size_t)(t0 + i) + 1] = qh;
-        }
+        rej = !acc;
       }
-      if (!acc && stop == K) stop = i;
-      if (greedy && stop < K) break;  // greedy rows after the stop carry no probabilities to fill
+      const unsigned m = __ballot_sync(kFull, rej);
+      if (m) {
+        stop = j0 + __ffs(m) - 1;
+        if (greedy) break;  // greedy rows carry no probabilities to fill in
+        // sampled slots after the stop still write their probabilities
+        for (j0 += 32; j0 < K; j0 += 32) {
+          const int i2 = j0 + lane;
+          if (i2 >= K) continue;
+          const int x = P.tokens[d0 + i2];
+          const bool bad = x < 0 || x >= P.V;
+          if (bad) atomicOr(P.status, SV_DATA_BAD_TOKEN);
+          const RowComb tr = combine_row(P.ts, P.R_t, t0 + i2, P.S);
+          if (!(tr.S > 0.0)) atomicOr(P.status, SV_DATA_EMPTY_ROW);
+          float ph = -1.f, qh = -1.f;
+          if (!bad) {
+            const float ap = fmaf(tr.zx, P.c, -tr.Mc);
+            ph = __fdiv_rn(exp2f(ap), (float)tr.S);
+            qh = 1.f;
+            if (P.ds) {
+              const RowComb dr = combine_row(P.ds, R_d, d0 + i2, P.S);
+              if (!(dr.S > 0.0)) atomicOr(P.status, SV_DATA_EMPTY_ROW);
+              qh = __fdiv_rn(exp2f(fmaf(dr.zx, P.c, -dr.Mc)), (float)dr.S);
+            }
+          }
+          if (P.out_probs) {
+            P.out_probs[2 * (size_t)(t0 + i2)] = ph;
+            P.out_probs[2 * (size_t)(t0 + i2) + 1] = qh;
+          }
+        }
+        break;
+      }
     }
-    for (int j = 0; j < stop; ++j) P.out_tokens[t0 + j] = P.tokens[d0 + j];
+    for (int j = lane; j < stop; j += 32) P.out_tokens[t0 + j] = P.tokens[d0 + j];
+    if (greedy && P.out_probs)
+      for (int j = lane; j <= K; j += 32) {  // greedy rows, the bonus row included
+        P.out_probs[2 * (size_t)(t0 + j)] = -1.f;
+        P.out_probs[2 * (size_t)(t0 + j) + 1] = -1.f;
+      }
+    if (lane != 0) continue;
     P.out_len[b] = stop + 1;
     Job job;
     job.row = -1;
@@ -374,12 +417,6 @@ __global__ void __launch_bounds__(kT) decide_kernel(DecideParams P) {
     if (greedy) {
       const RowComb tr = combine_row(P.ts, P.R_t, t0 + stop, P.S);
       P.out_tokens[t0 + stop] = tr.ai == INT_MAX ? 0 : tr.ai;
-      if (P.out_probs) {
-        for (int j = stop; j <= K; ++j) {  // rows the loop did not reach, and the bonus row
-          P.out_probs[2 * (size_t)(t0 + j)] = -1.f;
-          P.out_probs[2 * (size_t)(t0 + j) + 1] = -1.f;
-        }
-      }
     } else {
       const RowComb tr = combine_row(P.ts, P.R_t, t0 + stop, P.S);
       job.row = t0 + stop;
@@ -445,7 +482,7 @@ __device__ void tile_totals(const Slice& sl, const Job& J, int kind, float c, fl
     if (lane == 0) wt[l * kW + warp] = ts;
   };
   if constexpr (VEC) {
-    constexpr int kU = 4;
+    constexpr int kU = SV_VS_LOADS;
     const uint4 ninf = DT == 1 ? make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u)
                                : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
     for (int l0 = 0; l0 < ntiles; l0 += kU) {
@@ -854,7 +891,7 @@ sv_status sv_vshard_decide(const sv_shard_stat* target_stats, const sv_shard_sta
   P.out_probs = out_probs;
   P.jobs = static_cast<Job*>(jobs);
   P.status = status;
-  decide_kernel<<<grid_for((B + kT - 1) / kT, 152), kT, 0, static_cast<cudaStream_t>(cuda_stream)>>>(P);
+  decide_kernel<<<grid_for((B + kW - 1) / kW, kStatGrid), kT, 0, static_cast<cudaStream_t>(cuda_stream)>>>(P);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
