@@ -191,6 +191,22 @@ sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype, int32_t 
 int32_t sv_set_cluster_rows(int32_t rows);
 
 /*
+ * A third kernel takes one-hot batches (draft_logits NULL, as from the n-gram
+ * or suffix proposer) of short rows that the cluster kernel does not: one
+ * CTA per target row streams its row with register loads, takes the row's
+ * decision, and the request's last row commits it, drawing from the stop row
+ * read once more (from L2 at these sizes). It runs for rows of at most
+ * `bytes` bytes (V * element size, and at most 1 MiB), 16-byte aligned with
+ * V * element size a multiple of 16, in spec_verify (greedy requests of
+ * such a batch included); the filtered and no-allocation entry points keep
+ * the persistent kernel. Sets the process-wide limit (0: never) and returns the
+ * previous one; the initial value is SV_ONEHOT_ROW_BYTES_DEFAULT. Negative
+ * values are ignored (the call then only returns the current limit).
+ */
+#define SV_ONEHOT_ROW_BYTES_DEFAULT 131072 /* 128 KiB */
+int32_t sv_set_onehot_row_bytes(int32_t bytes);
+
+/*
  * Top-k / top-p filtered verify-and-commit ("投机解码从零实现", §5.4
  * "采样策略对比": top-k and nucleus rejection sampling keep the output
  * distribution when the same filter is applied to the target and the draft

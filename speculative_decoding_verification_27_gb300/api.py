@@ -24,6 +24,7 @@ SV_DATA_EMPTY_ROW = 0x4
 SV_DATA_BAD_MODE = 0x8
 SV_DATA_DEGENERATE_RESIDUAL = 0x10
 SV_DEV_COPY_TIMEOUT = 0x20
+SV_ONEHOT_ROW_BYTES_DEFAULT = 128 * 1024  # sv_set_onehot_row_bytes' initial limit
 
 HEADER = os.path.join(ROOT, "include", "spec_verify.h")
 
@@ -420,6 +421,16 @@ def spec_verify_filtered(target: torch.Tensor, draft: Optional[torch.Tensor], dr
             _stream(stream))
     _check("spec_verify_filtered", st)
     return out_tokens, out_len, out_probs
+
+
+def sv_set_onehot_row_bytes(nbytes: int) -> int:
+    """Largest row (V * element size, in bytes) that spec_verify runs with
+    the one-CTA-per-row kernel for one-hot batches (0: never; negative: only
+    read); returns the previous limit. Process-wide."""
+    lib = load()
+    lib.sv_set_onehot_row_bytes.argtypes = [ctypes.c_int32]
+    lib.sv_set_onehot_row_bytes.restype = ctypes.c_int32
+    return int(lib.sv_set_onehot_row_bytes(int(nbytes)))
 
 
 def sv_set_cluster_rows(rows: int) -> int:

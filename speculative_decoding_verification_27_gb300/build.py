@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(PKG, "libspecverify.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
 SOURCES = ["spec_verify.cu", "ngram.cu", "suffix.cu", "metrics.cu", "filter.cu", "candidates.cu",
-           "vshard.cu", "cluster.cu", "greedy.cu", "fcommit.cu"]
+           "vshard.cu", "cluster.cu", "greedy.cu", "fcommit.cu", "onehot.cu"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -47,6 +47,7 @@
 #include "sv_filter.cuh"
 #include "sv_cluster.cuh"
 #include "sv_greedy.cuh"
+#include "sv_onehot.cuh"
 
 namespace sv {
 
@@ -2027,6 +2028,10 @@ static sv_status check_verify_args(const void* target, const void* draft, sv_dty
 // Workspaces holding at most this many target rows take the cluster kernel.
 static std::atomic<int> g_cluster_rows{SV_CLUSTER_ROWS_DEFAULT};
 
+// One-hot batches (no draft rows) with rows of at most this many bytes take
+// the one-CTA-per-row kernel when the cluster kernel does not.
+static std::atomic<int> g_onehot_row_bytes{SV_ONEHOT_ROW_BYTES_DEFAULT};
+
 static sv_status run_verify(const void* target, const void* draft, sv_dtype dtype, int32_t V,
                             int32_t B, const int32_t* draft_tokens, const int32_t* cu_draft,
                             const uint8_t* mode, const float* uniforms, float temperature,
@@ -2130,6 +2135,31 @@ static sv_status run_verify(const void* target, const void* draft, sv_dtype dtyp
     C.nvec = (int)(((size_t)V * es) / 16);
     C.vp = 0;
     e = launch_cluster_verify(C, dtype == SV_BF16 ? 1 : 0, st);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  }
+  if (vec && !thr && !P.draft && row_tiles &&
+      (long long)V * (long long)es <= (long long)g_onehot_row_bytes.load(std::memory_order_relaxed) &&
+      (size_t)V * es / 16 <= (size_t)kOneHotMaxVec) {
+    // Short rows and one-hot proposals: one CTA per row, no claims, no ring.
+    RParams R;
+    R.target = target;
+    R.V = V;
+    R.B = B;
+    R.draft_tokens = draft_tokens;
+    R.cu = cu_draft;
+    R.mode = P.mode;
+    R.uniforms = uniforms;
+    R.c = P.c;
+    R.out_tokens = out_tokens;
+    R.out_len = out_len;
+    R.out_probs = P.out_probs;
+    R.status = &P.ws->status;
+    R.arrive = P.req_state;
+    R.rows = reinterpret_cast<RRow*>(P.rows);
+    R.row_cap = P.row_cap;
+    R.greedy_all = greedy_all;
+    R.nvec = (int)(((size_t)V * es) / 16);
+    e = launch_onehot_verify(R, dtype == SV_BF16 ? 1 : 0, st);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
   }
   if (thr) {
@@ -2363,6 +2393,11 @@ const char* sv_status_string(sv_status status) {
     case SV_ERR_DATA: return "SV_ERR_DATA";
   }
   return "SV_ERR_UNKNOWN";
+}
+
+int32_t sv_set_onehot_row_bytes(int32_t bytes) {
+  if (bytes < 0) return sv::g_onehot_row_bytes.load();
+  return sv::g_onehot_row_bytes.exchange(bytes);
 }
 
 int32_t sv_set_cluster_rows(int32_t rows) {

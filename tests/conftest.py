@@ -37,10 +37,14 @@ def cuda_lib():
 @pytest.fixture(params=["persistent", "cluster"])
 def kernel_path(request, cuda_lib):
     """Runs the test once with each verify kernel: the persistent kernel
-    (cluster threshold 0) and the one-cluster-per-row kernel (threshold above
-    any test's rows; rows that are not 16-byte vectors still take the
-    persistent kernel). The threshold is restored afterwards."""
+    (cluster threshold 0, one-hot row limit 0) and the one-cluster-per-row
+    kernel (threshold above any test's rows; rows that are not 16-byte
+    vectors still take the persistent kernel). The thresholds are restored
+    afterwards. The one-hot row kernel has its own tests."""
     from speculative_decoding_verification_27_gb300 import api
-    prev = api.sv_set_cluster_rows(0 if request.param == "persistent" else 1 << 20)
+    persistent = request.param == "persistent"
+    prev = api.sv_set_cluster_rows(0 if persistent else 1 << 20)
+    prev_oh = api.sv_set_onehot_row_bytes(0 if persistent else -1)
     yield request.param
     api.sv_set_cluster_rows(prev)
+    api.sv_set_onehot_row_bytes(prev_oh)

@@ -387,3 +387,92 @@ def test_greedy_entry_ties_empty_rows_and_two_lookup_rounds(cuda_lib, dtype):
     tok2, ln2 = api.spec_verify_greedy(db.target, db.draft_tokens, db.cu_draft, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(ln2.cpu(), torch.from_numpy(ln)) and api.sv_check_status(ws) == api.SV_DATA_BAD_TOKEN
+
+
+# --------------------------------------------------------------------------
+# The one-CTA-per-row kernel for one-hot batches
+# --------------------------------------------------------------------------
+@pytest.fixture
+def onehot_kernel(cuda_lib):
+    """Routes one-hot batches of short rows to the one-CTA-per-row kernel
+    (no cluster kernel); restores the thresholds afterwards."""
+    prev = api.sv_set_cluster_rows(0)
+    prev_oh = api.sv_set_onehot_row_bytes(api.SV_ONEHOT_ROW_BYTES_DEFAULT)
+    yield
+    api.sv_set_cluster_rows(prev)
+    api.sv_set_onehot_row_bytes(prev_oh)
+
+
+@pytest.mark.parametrize("dtype,V", [("fp32", 3000), ("fp32", 32000), ("bf16", 8200), ("bf16", 65536)])
+def test_one_hot_kernel_ragged_mixed(onehot_kernel, dtype, V):
+    """Ragged K (0, 1, 31 and beyond 31, whose rows count their progress
+    instead of tracking per-slot bits), half the requests greedy, one-hot
+    proposals: every output equals the oracle's."""
+    Ks = [0, 1, 3, 31, 32, 40, 7, 2, 5, 0, 4, 6]
+    b = W.gaussian_sampling(seed=310 + V, B=len(Ks), K=Ks, V=V, sigma=2.0, draft_sigma=0.5, T=0.8, dtype=dtype)
+    b.draft = None
+    b.mode = np.array([0, 1] * (len(Ks) // 2), np.uint8)
+    rep, _, _ = _run(b)
+    assert rep.mismatched_requests == 0, rep.as_dict()
+
+
+def test_one_hot_kernel_config4(onehot_kernel):
+    """Config 4's verify (n-gram proposals, fp32 V=32000) on the one-hot
+    kernel, the path spec_verify takes for it by default."""
+    import oracle
+    nb = W.config4_histories(seed=104)
+    o_out, o_cnt, _ = oracle.ngram_propose(nb.histories, nb.hist_len, nb.min_n, nb.max_n, nb.max_tokens)
+    vb = W.config4_verify(seed=104, proposals=o_out, counts=o_cnt)
+    rep, _, _ = _run(vb, flag_budget=parity.FLAG_BUDGET, draw_flags_in_budget=False)  # flat rows
+    assert rep.mismatched_requests <= max(1, 1e-4 * rep.rows)
+
+
+def test_one_hot_kernel_data_errors_and_rerun(onehot_kernel):
+    """A token out of range and decreasing offsets set their status bits;
+    the workspace stays usable and a rerun is bit-identical."""
+    b = W.gaussian_sampling(seed=320, B=8, K=3, V=512, sigma=1.0, draft_sigma=0.5, T=1.0)
+    b.draft = None
+    ws = api.new_workspace(b.B, b.R_t, b.V)
+    db = parity.to_device(b)
+    bad = db.draft_tokens.clone()
+    bad[2] = 512
+    api.spec_verify(db.target, None, bad, db.cu_draft, db.uniforms, 1.0, workspace=ws)
+    assert api.sv_check_status(ws) & api.SV_DATA_BAD_TOKEN
+    cu_bad = db.cu_draft.clone()
+    cu_bad[3] = 1
+    api.spec_verify(db.target, None, db.draft_tokens, cu_bad, db.uniforms, 1.0, workspace=ws)
+    assert api.sv_check_status(ws) & api.SV_DATA_BAD_OFFSETS
+    g1 = parity.gpu_verify(db, ws)
+    g2 = parity.gpu_verify(db, ws)
+    rep = parity.compare(b, g1, parity.oracle_verify(b))
+    assert rep.mismatched_requests == 0, rep.as_dict()
+    assert np.array_equal(g1[1], g2[1]) and np.array_equal(g1[2], g2[2])
+    t0 = b.cu_draft[:-1] + np.arange(b.B)
+    for i in range(b.B):
+        assert np.array_equal(g1[0][t0[i]:t0[i] + g1[1][i]], g2[0][t0[i]:t0[i] + g2[1][i]])
+    assert api.sv_check_status(ws) == 0
+
+
+def test_one_hot_kernel_chi_square(onehot_kernel):
+    """1e6 rounds, V=16, K=1, one-hot proposals drawn from some q: accepting
+    x̂ with probability p(x̂) and otherwise drawing from p without x̂ emits a
+    first token that follows p, and accepts with probability sum q p."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(13)
+    V, N = 16, 1_000_000
+    zp = rng.normal(0, 1.5, V).astype(np.float32)
+    zb = rng.normal(0, 1.5, V).astype(np.float32)
+    p = softmax(zp.astype(np.float64))
+    q = softmax(rng.normal(0, 1.0, V))
+    cu = np.arange(N + 1, dtype=np.int32)
+    toks = np.searchsorted(np.cumsum(q), rng.random(N), side="right").clip(0, V - 1).astype(np.int32)
+    target = torch.from_numpy(np.stack([zp, zb])).cuda().repeat(N, 1)
+    tok, ln, _ = api.spec_verify(target, None, torch.from_numpy(toks).cuda(), torch.from_numpy(cu).cuda(),
+                                 torch.from_numpy(W.uniforms_for(cu, seed=22)).cuda(), 1.0, want_probs=False)
+    first = tok.view(N, 2)[:, 0].cpu().numpy()
+    hist = np.bincount(first, minlength=V)
+    chi2 = float(((hist - N * p) ** 2 / (N * p)).sum())
+    assert chi2 < 37.70, chi2
+    alpha = float((q * p).sum())
+    acc = (ln.cpu().numpy() == 2).mean()
+    assert abs(acc - alpha) < 5 * np.sqrt(alpha * (1 - alpha) / N)
