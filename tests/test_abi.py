@@ -122,3 +122,20 @@ def test_python_binding_rejects_host_tensors(lib):
                                out_tokens=torch.zeros(3, dtype=torch.int32),
                                out_len=torch.zeros(1, dtype=torch.int32),
                                workspace=torch.zeros(256, dtype=torch.uint8))
+
+
+def test_kernel_choice_knobs_round_trip(lib):
+    """The process-wide thresholds that pick the cluster kernel and the
+    one-hot row kernel are host state: negative values only read them, any
+    other value sets them and returns the previous one."""
+    assert api.sv_set_cluster_rows(-1) == 64
+    assert api.sv_set_onehot_row_bytes(-1) == api.SV_ONEHOT_ROW_BYTES_DEFAULT == 128 * 1024
+    try:
+        assert api.sv_set_cluster_rows(7) == 64
+        assert api.sv_set_cluster_rows(-5) == 7
+        assert api.sv_set_onehot_row_bytes(0) == 128 * 1024
+        assert api.sv_set_onehot_row_bytes(-1) == 0
+    finally:
+        api.sv_set_cluster_rows(64)
+        api.sv_set_onehot_row_bytes(api.SV_ONEHOT_ROW_BYTES_DEFAULT)
+    assert api.sv_set_cluster_rows(-1) == 64 and api.sv_set_onehot_row_bytes(-1) == 128 * 1024
