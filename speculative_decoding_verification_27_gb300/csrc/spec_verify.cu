@@ -2293,6 +2293,13 @@ sv_status spec_verify_filtered(const void* target_logits, const void* draft_logi
   const size_t es = dtype == SV_FP32 ? 4 : 2;
   if ((uintptr_t)target_logits % es || (draft_logits && (uintptr_t)draft_logits % es))
     return SV_ERR_INVALID_ARG;
+  // Every check of the verify step too, before the thresholds are enqueued:
+  // a rejected call enqueues nothing.
+  const sv_status chk = sv::check_verify_args(target_logits, draft_logits, dtype, V, B, draft_tokens,
+                                              cu_draft, uniforms, temperature, out_tokens, out_len,
+                                              out_probs, 0);
+  if (chk != SV_OK) return chk;
+  if (workspace_bytes - fb < sv::ws_layout(B, V).rows + sizeof(sv::RowRec)) return SV_ERR_INVALID_ARG;
   sv::FtParams fp;
   fp.target = target_logits;
   fp.draft = draft_logits;

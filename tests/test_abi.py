@@ -139,3 +139,39 @@ def test_kernel_choice_knobs_round_trip(lib):
         api.sv_set_cluster_rows(64)
         api.sv_set_onehot_row_bytes(api.SV_ONEHOT_ROW_BYTES_DEFAULT)
     assert api.sv_set_cluster_rows(-1) == 64 and api.sv_set_onehot_row_bytes(-1) == 128 * 1024
+
+
+def _filtered(lib, **kw):
+    P, i32, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+    lib.spec_verify_filtered.argtypes = [P, P, ctypes.c_int, i32, i32, i32, P, P, P, P, f32, i32, f32,
+                                         P, P, P, P, ctypes.c_size_t, P]
+    lib.spec_verify_filtered.restype = ctypes.c_int
+    a = dict(target=FAKE, draft=None, dtype=1, V=128, B=2, R_t=6, toks=FAKE, cu=FAKE, mode=None, u=FAKE,
+             T=1.0, k=10, p=0.9, ot=FAKE, ol=FAKE, op=None, ws=FAKE, wsb=1 << 20, st=None)
+    a.update(kw)
+    return lib.spec_verify_filtered(a["target"], a["draft"], a["dtype"], a["V"], a["B"], a["R_t"], a["toks"],
+                                    a["cu"], a["mode"], a["u"], a["T"], a["k"], a["p"], a["ot"], a["ol"],
+                                    a["op"], a["ws"], a["wsb"], a["st"])
+
+
+def test_spec_verify_filtered_host_validation(lib):
+    """Every argument the filtered step checks is checked before its first
+    kernel: without a GPU a call that got past the checks would fail in
+    CUDA (SV_ERR_CUDA), so each rejection here comes first."""
+    E = api.SV_ERR_INVALID_ARG
+    assert _filtered(lib, B=0) == api.SV_OK
+    assert _filtered(lib, k=-1) == E
+    assert _filtered(lib, p=0.0) == E
+    assert _filtered(lib, R_t=1) == E                 # fewer rows than requests
+    assert _filtered(lib, T=0.0) == E
+    assert _filtered(lib, ws=None) == E
+    assert _filtered(lib, ws=MISALIGNED) == E
+    assert _filtered(lib, wsb=64) == E                # smaller than the thresholds' part
+    need = int(lib.spec_verify_filtered_workspace_size(2, 6, 128))
+    assert need > 0
+    assert _filtered(lib, wsb=need - api.spec_verify_workspace_size(2, 6, 128) + 16) == E  # no room for the verify part
+    assert _filtered(lib, ot=None) == E               # checked before the thresholds are enqueued
+    assert _filtered(lib, ol=None) == E
+    assert _filtered(lib, u=None) == E
+    assert _filtered(lib, cu=MISALIGNED) == E
+    assert _filtered(lib, op=MISALIGNED) == E
