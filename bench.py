@@ -44,8 +44,8 @@ WORKLOAD = ("sampling verify B=256 K=7 V=151936 bf16 T=0.7, peaked rank-score ro
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per verify launch on this workload from one ncu
 # capture, valid only for the kernel sources whose hash is recorded with it.
-TRAFFIC = {"sources_sha256": "4a6f1a9d056df92508c903aaf4259328ee778c5b14cdff4fe5d1d9cae94f432f",
-           "bytes_per_launch": 1235004672 + 4239872,
+TRAFFIC = {"sources_sha256": "07cd1b2605df1b3f5e0fb7aecfd57cf87d31deba716596232bf994a0c9b2cb35",
+           "bytes_per_launch": 1235357440 + 4756224,
            "profile": "profiles/verify_kernel_sampling_B256_K7_V151936_bf16.md"}
 
 
