@@ -16,6 +16,12 @@
 // CTA draws from the stop row's list (r at the listed tokens, put in
 // vocabulary order, scanned in double-float). Requests it cannot finish are
 // left to the streaming verify kernel, which then skips the others.
+//
+// Flags in the workspace, all written in stream order (no CTA waits): each
+// CTA writes done[b] (1: committed here); a CTA that leaves its request sets
+// need_slow, which the verify kernel reads on entry (0: it returns at once)
+// and its last CTA clears; CTA 0 clears rows_left, the word through which the
+// one-warp threshold kernel told the CTA threshold kernel of rows it left.
 #include "../../include/spec_verify.h"
 #include "sv_device.cuh"
 #include "sv_filter.cuh"
