@@ -155,7 +155,7 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
  * bonus row, emit that row's argmax. Bit-exact; no temperature, no
  * uniforms. Arguments as for spec_verify. On 16-byte-aligned rows whose
  * byte length is a multiple of 16, one CTA per target row streams the row
- * (eight 16-byte loads in flight per thread) and the request's last row
+ * (sixteen 16-byte loads in flight per thread) and the request's last row
  * commits it; other rows take the persistent kernel.
  */
 sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype, int32_t V, int32_t B,
@@ -164,8 +164,8 @@ sv_status spec_verify_greedy(const void* target_logits, sv_dtype dtype, int32_t 
                              size_t workspace_bytes, void* cuda_stream);
 
 /*
- * Which kernel runs spec_verify. Both compute the same step (the rule
- * above):
+ * Which kernel runs spec_verify. Each computes the same step (the rule
+ * above); the third, for one-hot batches, is described after this one:
  *   - a persistent kernel, a fixed number of CTAs per SM, streams rows
  *     through a shared-memory ring and commits each request as soon as its
  *     stop slot is known; the default for large batches;
